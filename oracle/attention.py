@@ -1,0 +1,329 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or run
+anything under ``oracle/``.  The CUDA library never calls it and shares no code
+with it.
+
+Sources (the three web pages this implementation follows):
+
+* [FA2-review]  "FlashAttention-2: Faster Attention with Better Parallelism and
+  Work Partitioning" (paper review page): the flowchart under "프레임워크 개요"
+  (Q,K,V in HBM -> tiles -> QK^T + online softmax statistics -> P V ->
+  one final rescale -> O and log-sum-exp), the "Methods" section (defer the
+  1/rowsum scaling to the end, keep only the log-sum-exp for the backward
+  pass), "핵심 구성요소" (skip blocks entirely above the causal diagonal; the
+  backward pass recomputes with the stored log-sum-exp), the glossary
+  ("Online softmax", "Log-sum-exp (LSE)"), and the table "기존 접근법의 한계"
+  naming standard (PyTorch) attention, which materialises the N x N matrix.
+* [FA3-8.3]  "8.3 FlashAttention-3": section 5.1 (block quantization, one
+  scale factor per block), section 5.2 (incoherent processing: multiply Q and
+  K by a random orthogonal matrix built from a Hadamard transform with +-1
+  entries).
+* [Triton07]  "Triton 07: Flash Attention v3": section "Method" (un-scaled
+  accumulation, exp2), the FP8 block-scaling + Hadamard item under the
+  "Hopper" future-work list.
+
+What this file computes, and how each function is pinned to something other
+than itself, is listed per function.  All floating point is fp64 unless a
+function is explicitly about the fp32/E4M3 encodings.
+
+Readings where the pages are silent (each also listed in the design doc):
+
+* LSE is the natural log of the sum of exp of the *scaled* scores.
+* Causal masking is top-left aligned: key j is visible to query i iff j <= i.
+* The softmax scale is the caller's (1/sqrt(d) in every workload).
+* The backward pass is for the loss L = sum(O * dO), i.e. dO is the incoming
+  gradient of O.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional, Sequence, Tuple
+
+import numpy as np
+
+__all__ = [
+    "scores", "allowed_mask", "masked_softmax", "attention_head", "attention",
+    "attention_rows", "online_softmax_attention_head", "attention_backward_head",
+    "attention_backward", "E4M3_MAX", "e4m3_decode", "e4m3_encode", "hadamard_matrix",
+    "rotation_matrix", "quantize_blocks", "dequantize_blocks", "rmse",
+]
+
+
+# ---------------------------------------------------------------------------
+# Forward: the plain definition ("standard attention" in [FA2-review])
+# ---------------------------------------------------------------------------
+
+def scores(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """S = scale * Q K^T for one head.  q: [Nq, d], k: [Nk, d] -> [Nq, Nk]."""
+    return scale * (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T)
+
+
+def allowed_mask(nq: int, nk: int, causal: bool) -> np.ndarray:
+    """Boolean [nq, nk]; causal keeps key j for query i iff j <= i (top-left)."""
+    if not causal:
+        return np.ones((nq, nk), dtype=bool)
+    return np.arange(nk)[None, :] <= np.arange(nq)[:, None]
+
+
+def masked_softmax(S: np.ndarray, allowed: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Row softmax over the allowed entries.
+
+    Returns (P, LSE) with LSE_i = log(sum_{j allowed} exp(S_ij)) (natural log,
+    glossary entry "Log-sum-exp" of [FA2-review]) and P_ij = exp(S_ij - LSE_i)
+    on allowed entries, 0 elsewhere.  The row maximum is subtracted before
+    exponentiating only to keep exp() in range; it cancels exactly.
+    """
+    Sm = np.where(allowed, S, -np.inf)
+    mx = np.max(Sm, axis=1, keepdims=True)
+    e = np.where(allowed, np.exp(Sm - mx), 0.0)
+    rowsum = e.sum(axis=1, keepdims=True)
+    lse = (mx + np.log(rowsum))[:, 0]
+    P = e / rowsum
+    return P, lse
+
+
+def attention_head(q, k, v, causal: bool, scale: float):
+    """O = softmax(scale Q K^T, masked) V for one head; returns (O, LSE, P)."""
+    S = scores(q, k, scale)
+    P, lse = masked_softmax(S, allowed_mask(S.shape[0], S.shape[1], causal))
+    O = P @ np.asarray(v, np.float64)
+    return O, lse, P
+
+
+def attention(q, k, v, causal: bool, scale: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Batched plain attention.  q,k,v: [B,H,N,d] -> O [B,H,N,d], LSE [B,H,N]."""
+    q = np.asarray(q, np.float64)
+    B, H, N, d = q.shape
+    O = np.empty((B, H, N, v.shape[-1]), np.float64)
+    L = np.empty((B, H, N), np.float64)
+    for b in range(B):
+        for h in range(H):
+            O[b, h], L[b, h], _ = attention_head(q[b, h], k[b, h], v[b, h], causal, scale)
+    return O, L
+
+
+def attention_rows(q, k, v, rows: Sequence[int], causal: bool, scale: float):
+    """Plain attention for selected query rows of one head (q,k,v: [N,d]).
+
+    Row i needs only q_i and all of K, V, so large workloads can be checked on
+    sampled rows.  Returns (O_rows [len(rows), d], LSE_rows [len(rows)]).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    rows = np.asarray(rows, dtype=np.int64)
+    S = scale * (q[rows] @ k.T)
+    allowed = np.ones_like(S, dtype=bool)
+    if causal:
+        allowed = np.arange(k.shape[0])[None, :] <= rows[:, None]
+    P, lse = masked_softmax(S, allowed)
+    return P @ v, lse
+
+
+# ---------------------------------------------------------------------------
+# Forward: the tiled online-softmax recurrence, in the pages' order
+# ---------------------------------------------------------------------------
+
+def online_softmax_attention_head(q, k, v, causal: bool, scale: float, block: int):
+    """Tiled attention with online softmax, fp64, following [FA2-review].
+
+    Steps, for each block of ``block`` query rows (flowchart "프레임워크
+    개요" and section "Methods"):
+      1. load the Q tile;
+      2. for each K/V tile (tiles entirely above the causal diagonal are
+         skipped, "핵심 구성요소" causal-masking item):
+           S = scale Q_tile K_tile^T, masked;
+           m_new = max(m, rowmax(S));
+           P~ = exp(S - m_new);
+           l = exp(m - m_new) l + rowsum(P~);
+           O~ = exp(m - m_new) O~ + P~ V_tile     (unnormalised);
+           m = m_new;
+      3. rescale once at the end: O = O~ / l;
+      4. write O and LSE = m + log(l).
+    Pinned by equality with ``attention_head`` (the plain definition) to
+    1e-12 for several block sizes, in tests/test_oracle.py.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    N, dv = q.shape[0], v.shape[1]
+    Nk = k.shape[0]
+    O = np.zeros((N, dv))
+    LSE = np.zeros(N)
+    for r0 in range(0, N, block):
+        r1 = min(N, r0 + block)
+        qt = q[r0:r1]
+        m = np.full(r1 - r0, -np.inf)
+        l = np.zeros(r1 - r0)
+        acc = np.zeros((r1 - r0, dv))
+        for c0 in range(0, Nk, block):
+            c1 = min(Nk, c0 + block)
+            if causal and c0 > r1 - 1:
+                break  # this and every later K/V tile lies above the diagonal
+            S = scale * (qt @ k[c0:c1].T)
+            if causal:
+                ok = np.arange(c0, c1)[None, :] <= np.arange(r0, r1)[:, None]
+                S = np.where(ok, S, -np.inf)
+            m_new = np.maximum(m, S.max(axis=1))
+            alpha = np.exp(m - m_new)           # exp(-inf) = 0 on the first tile
+            Pt = np.exp(S - m_new[:, None])
+            l = alpha * l + Pt.sum(axis=1)
+            acc = alpha[:, None] * acc + Pt @ v[c0:c1]
+            m = m_new
+        O[r0:r1] = acc / l[:, None]
+        LSE[r0:r1] = m + np.log(l)
+    return O, LSE
+
+
+# ---------------------------------------------------------------------------
+# Backward: closed-form gradients of L = sum(O * dO)
+# ---------------------------------------------------------------------------
+
+def attention_backward_head(q, k, v, do, causal: bool, scale: float):
+    """dQ, dK, dV for one head, recomputing P from the definition.
+
+    [FA2-review] "핵심 구성요소" (backward item) recomputes P from the stored
+    log-sum-exp; mathematically P is the same softmax as in the forward pass,
+    so the oracle rebuilds it from the definition:
+      dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij;
+      dS = P o (dP - D);  dQ = scale dS K;  dK = scale dS^T Q.
+    Pinned by central finite differences of L and by closed forms for Q = 0
+    in tests/test_oracle.py.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    _, _, P = attention_head(q, k, v, causal, scale)
+    dV = P.T @ do
+    dP = do @ v.T
+    D = np.sum(P * dP, axis=1, keepdims=True)
+    dS = P * (dP - D)
+    dQ = scale * (dS @ k)
+    dK = scale * (dS.T @ q)
+    return dQ, dK, dV, dS
+
+
+def attention_backward(q, k, v, do, causal: bool, scale: float, heads=None):
+    """Batched backward.  Returns dQ, dK, dV as [B,H,N,d] fp64.
+
+    ``heads`` (optional iterable of (b, h)) restricts the work to those heads;
+    the other entries are left as NaN.
+    """
+    q = np.asarray(q, np.float64)
+    B, H, N, d = q.shape
+    dQ = np.full(q.shape, np.nan)
+    dK = np.full(q.shape, np.nan)
+    dV = np.full(q.shape, np.nan)
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads:
+        dQ[b, h], dK[b, h], dV[b, h], _ = attention_backward_head(
+            q[b, h], k[b, h], v[b, h], do[b, h], causal, scale)
+    return dQ, dK, dV
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 block quantization and the randomized Hadamard rotation
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0  # largest finite E4M3 value: 1.75 * 2^8
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Decode E4M3 ("fn" variant: no infinities, 0x7F/0xFF are NaN) to fp64.
+
+    Bit layout: sign (1) | exponent (4, bias 7) | mantissa (3).  Exponent 0
+    is subnormal: value = m/8 * 2^-6.  Written from the format definition.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x32: np.ndarray) -> np.ndarray:
+    """Round fp32 values to E4M3 (nearest, ties to even), saturating at +-448.
+
+    Uses torch's float8_e4m3fn cast as the library rounding routine after a
+    clamp to +-448 (the "satfinite" reading).  Pinned against a brute-force
+    nearest-code search over all 256 codes in tests/test_oracle.py.
+    """
+    import torch
+    x = np.clip(np.asarray(x32, np.float32), -E4M3_MAX, E4M3_MAX)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def hadamard_matrix(d: int) -> np.ndarray:
+    """Sylvester Hadamard matrix H_d (d a power of two), entries +-1."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    H = np.ones((1, 1))
+    while H.shape[0] < d:
+        H = np.block([[H, H], [H, -H]])
+    return H
+
+
+def rotation_matrix(signs) -> np.ndarray:
+    """R = H_d diag(signs) / sqrt(d): orthogonal, so (Q R)(K R)^T = Q K^T.
+
+    [FA3-8.3] section 5.2 multiplies Q and K by a random orthogonal matrix made
+    from a Hadamard transform; the random part is the +-1 sign vector, drawn
+    by the workload generator and passed in.
+    """
+    s = np.asarray(signs, np.float64)
+    d = s.shape[0]
+    return hadamard_matrix(d) * s[None, :] / math.sqrt(d)
+
+
+def quantize_blocks(x, block_rows: int = 64, signs=None) -> Dict[str, np.ndarray]:
+    """Per-block E4M3 quantization of one tensor [B,H,N,d] ([FA3-8.3] 5.1).
+
+    For each (b, h) and each block of ``block_rows`` consecutive rows (the last
+    block may be shorter):
+      * optional rotation x <- x R (``signs`` given), computed in fp64 and
+        rounded to fp32;
+      * amax = max |x| over the block (fp32);
+      * s = amax / 448 as one IEEE fp32 division (s = 1 when amax = 0);
+      * code = E4M3(x / s), the division again in IEEE fp32.
+    Returns dict(codes uint8 [B,H,N,d], scales fp32 [B,H,ceil(N/block_rows)],
+    x32 = the fp32 values that were quantized).
+    """
+    x = np.asarray(x, np.float64)
+    B, H, N, d = x.shape
+    if signs is not None:
+        x = x @ rotation_matrix(signs)
+    x32 = x.astype(np.float32)
+    nb = (N + block_rows - 1) // block_rows
+    codes = np.empty(x.shape, np.uint8)
+    scales = np.empty((B, H, nb), np.float32)
+    for b in range(B):
+        for h in range(H):
+            for i in range(nb):
+                blk = x32[b, h, i * block_rows:(i + 1) * block_rows]
+                amax = np.float32(np.max(np.abs(blk))) if blk.size else np.float32(0)
+                s = np.float32(amax) / np.float32(E4M3_MAX) if amax > 0 else np.float32(1.0)
+                scales[b, h, i] = s
+                codes[b, h, i * block_rows:(i + 1) * block_rows] = e4m3_encode(
+                    (blk / np.float32(s)).astype(np.float32))
+    return {"codes": codes, "scales": scales, "x32": x32}
+
+
+def dequantize_blocks(codes, scales, block_rows: int = 64) -> np.ndarray:
+    """Inverse of ``quantize_blocks`` up to rounding: code value * block scale."""
+    vals = e4m3_decode(codes)
+    s = np.repeat(np.asarray(scales, np.float64), block_rows, axis=2)[:, :, :vals.shape[2]]
+    return vals * s[..., None]
+
+
+def rmse(a, b) -> float:
+    """Root-mean-square of (a - b) over all elements (absolute)."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.sqrt(np.mean((a - b) ** 2)))

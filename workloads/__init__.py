@@ -1,0 +1,133 @@
+"""Seeded synthetic workloads for exact attention.
+
+This module only draws numbers: shapes, seeds, distributions and the order of
+the draws.  It holds none of the attention arithmetic, so both the fp64 oracle
+(``oracle/``) and the CUDA path (``exact_attention_75_gb300``) can take their
+inputs from here without sharing any code of the method itself.
+
+Recipe (the same on every machine, because all draws come from a CPU
+``torch.Generator``):
+
+* ``torch.Generator().manual_seed(seed)``; fp32 standard normals drawn in the
+  order q, k, v, then dO (backward workloads only), each with shape [B,H,N,d].
+* optional multiplication of q, k, v by ``input_scale`` in fp32 (0.5 for the
+  d=128 bf16 forward workload);
+* optional outliers: after the normals, one uniform draw per element of q, k
+  and v (in that order); entries whose draw is < ``outlier_prob`` (0.001) are
+  multiplied by ``outlier_mult`` (20);
+* optional Hadamard sign vector: after everything else, ``d`` draws of
+  {0, 1} mapped to {+1, -1}; these are the random signs of the randomized
+  Hadamard rotation, passed to both sides as an input;
+* finally a cast to the workload dtype (fp16 / bf16) with round-to-nearest.
+
+The workloads themselves are the five shapes the attention kernels are
+measured on (fp16 and bf16 forward at d=64 and d=128, the bf16 backward, the
+FP8 forward with outliers), plus the sequence-length sweeps that keep B*N at
+16384 tokens.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, List, Optional
+
+import torch
+
+TOKENS_PER_SWEEP = 16384
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str            # "fwd", "bwd" or "fwd_fp8"
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str           # "fp16" or "bf16" (dtype of q, k, v, o, do)
+    causal: bool
+    input_scale: float = 1.0
+    outliers: bool = False
+    hadamard: bool = False
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale 1/sqrt(d) used by every workload."""
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return {"fp16": torch.float16, "bf16": torch.bfloat16}[self.dtype]
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    def fwd_flops(self) -> float:
+        """4*B*H*N^2*d, halved for causal attention."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        """2.5x the forward count."""
+        return 2.5 * self.fwd_flops()
+
+
+# The five measured workloads.
+TINY_FWD_FP16 = Workload("fwd_fp16_causal_b1h2n256d64", "fwd", 1, 2, 256, 64, "fp16", True)
+FWD_FP16_D64 = Workload("fwd_fp16_b4h16n4096d64", "fwd", 4, 16, 4096, 64, "fp16", True)
+FWD_BF16_D128 = Workload("fwd_bf16_b2h16n8192d128", "fwd", 2, 16, 8192, 128, "bf16", True,
+                         input_scale=0.5)
+BWD_BF16_D128 = Workload("bwd_bf16_causal_b2h16n8192d128", "bwd", 2, 16, 8192, 128, "bf16", True)
+FWD_FP8_D128 = Workload("fwd_fp8_causal_b2h16n8192d128", "fwd_fp8", 2, 16, 8192, 128, "bf16",
+                        True, outliers=True, hadamard=True)
+
+WORKLOADS = [TINY_FWD_FP16, FWD_FP16_D64, FWD_BF16_D128, BWD_BF16_D128, FWD_FP8_D128]
+
+
+def sweep_d64(causal: bool) -> List[Workload]:
+    """fp16 d=64 forward at N in {512..8192}, B = 16384 / N, H = 16."""
+    return [FWD_FP16_D64.with_(name=f"fwd_fp16_d64_n{n}", B=TOKENS_PER_SWEEP // n, N=n,
+                               causal=causal)
+            for n in (512, 1024, 2048, 4096, 8192)]
+
+
+def sweep_d128(causal: bool) -> List[Workload]:
+    """bf16 d=128 forward at N in {1024..16384} (powers of two), B = 16384 / N."""
+    return [FWD_BF16_D128.with_(name=f"fwd_bf16_d128_n{n}", B=TOKENS_PER_SWEEP // n, N=n,
+                                causal=causal)
+            for n in (1024, 2048, 4096, 8192, 16384)]
+
+
+def make_inputs(w: Workload, with_do: Optional[bool] = None) -> Dict[str, torch.Tensor]:
+    """Draw the seeded inputs of workload ``w`` on the CPU.
+
+    Returns a dict with ``q``, ``k``, ``v`` (and ``do`` for backward workloads)
+    as CPU tensors of the workload dtype, and ``signs`` (int8, length d, values
+    +-1) when the workload uses the randomized Hadamard rotation.
+    """
+    if with_do is None:
+        with_do = w.kind == "bwd"
+    g = torch.Generator().manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    names = ["q", "k", "v"] + (["do"] if with_do else [])
+    raw = {n: torch.randn(shape, generator=g, dtype=torch.float32) for n in names}
+    if w.input_scale != 1.0:
+        for n in ("q", "k", "v"):
+            raw[n] = raw[n] * w.input_scale
+    if w.outliers:
+        for n in ("q", "k", "v"):
+            u = torch.rand(shape, generator=g, dtype=torch.float32)
+            raw[n] = torch.where(u < 0.001, raw[n] * 20.0, raw[n])
+    out = {n: t.to(w.torch_dtype) for n, t in raw.items()}
+    if w.hadamard:
+        bits = torch.randint(0, 2, (w.d,), generator=g)
+        out["signs"] = (1 - 2 * bits).to(torch.int8)
+    return out
+
+
+def head_range(rank: int, world: int, BH: int) -> range:
+    """Contiguous share of the B*H independent heads given to ``rank``."""
+    per = (BH + world - 1) // world
+    lo = min(BH, rank * per)
+    return range(lo, min(BH, lo + per))
