@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on one GB300 per rank.
+
+One *step* is one pass of the whole hot path over one batch of the
+[B=2, H=16, N=8192, d=128] causal workload (the shape shared by the bf16
+forward, the bf16 backward and the FP8 forward workloads):
+
+  fwd      bf16 forward               attn_fwd          -> O, LSE
+  bwd      bf16 backward              attn_bwd          -> dQ, dK, dV
+  quant    E4M3 block quantization    attn_quantize_fp8 (q, k with Hadamard; v transposed)
+  fwd_fp8  FP8 forward                attn_fwd_fp8      -> O8, LSE8
+
+FLOPs are counted as 4*B*H*N^2*d per forward (halved for causal) and 2.5x that
+for the backward; the quantization pass counts no FLOPs.  ``value`` is the
+step's FLOPs divided by its device time (CUDA events on the launching stream),
+summed over ranks; the inputs (q, k, v, dO: 256 MiB) are larger than the
+129 MB L2, so no flush is inserted between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+``--impl reference`` times the fp64 CPU oracle instead (the slow plain
+definition, on the host cores, on a bounded sample of the same workload).
+Multi-GPU (torchrun): every rank runs its own full batch (weak scaling, no
+collective on the data path); ranks meet only at the timing barriers.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+WORKLOAD = wl.Workload("attn_step_bf16_causal_b2h16n8192d128", "bwd", 2, 16, 8192, 128, "bf16",
+                       True, hadamard=True)
+COMPONENTS = ("fwd", "bwd", "quant", "fwd_fp8")
+LAUNCHES = {"fwd": 1, "bwd": 3, "quant": 3, "fwd_fp8": 1}  # kernels per component call
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained",
+                                                      pk["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------ clocks -------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ GPU arm -------
+
+class Step:
+    """All buffers of one step, resident on the device."""
+
+    def __init__(self, attn, w: wl.Workload, dev, components):
+        self.attn, self.w, self.dev, self.components = attn, w, dev, components
+        inp = wl.make_inputs(w, with_do=True)
+        self.host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+        self.signs = inp["signs"].to(dev)
+        self.q, self.k, self.v, self.do = (self.host[n].to(dev) for n in ("q", "k", "v", "do"))
+        B, H, N, d = w.B, w.H, w.N, w.d
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        if "bwd" in components:
+            self.ws = torch.empty(attn.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                                  device=dev)
+            self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        if "quant" in components or "fwd_fp8" in components:
+            nb = (N + 63) // 64
+            self.q8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=dev)
+            self.k8 = torch.empty_like(self.q8)
+            self.v8t = torch.empty((B, H, d, N), dtype=torch.uint8, device=dev)
+            self.sq, self.sk, self.sv = (torch.empty((B, H, nb), dtype=torch.float32,
+                                                     device=dev) for _ in range(3))
+            self.o8 = torch.empty_like(self.q)
+            self.lse8 = torch.empty_like(self.lse)
+
+    def run(self, name):
+        a, w = self.attn, self.w
+        if name == "fwd":
+            a.fwd(self.q, self.k, self.v, causal=w.causal, scale=w.scale, out=self.o,
+                  lse=self.lse)
+        elif name == "bwd":
+            a.bwd(self.q, self.k, self.v, self.o, self.do, self.lse, causal=w.causal,
+                  scale=w.scale, workspace=self.ws, dq=self.dq, dk=self.dk, dv=self.dv)
+        elif name == "quant":
+            L = a.lib()
+            import ctypes
+            s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            B, H, N, d = w.B, w.H, w.N, w.d
+            for x, out, sc, sg, tr in ((self.q, self.q8, self.sq, self.signs, 0),
+                                       (self.k, self.k8, self.sk, self.signs, 0),
+                                       (self.v, self.v8t, self.sv, None, 1)):
+                st = L.attn_quantize_fp8(ctypes.c_void_p(x.data_ptr()),
+                                         ctypes.c_void_p(out.data_ptr()),
+                                         ctypes.c_void_p(sc.data_ptr()), B, H, N, d, 64,
+                                         ctypes.c_void_p(0 if sg is None else sg.data_ptr()),
+                                         tr, s)
+                if st != 0:
+                    raise a.AttnError("attn_quantize_fp8", st)
+        elif name == "fwd_fp8":
+            a.fwd_fp8(self.q8, self.k8, self.v8t, self.sq, self.sk, self.sv, causal=w.causal,
+                      scale=w.scale, out=self.o8, lse=self.lse8)
+
+    def outputs(self):
+        outs = [self.o, self.lse]
+        if "bwd" in self.components:
+            outs += [self.dq, self.dk, self.dv]
+        if "fwd_fp8" in self.components:
+            outs += [self.o8, self.lse8]
+        return outs
+
+
+def component_flops(w: wl.Workload):
+    return {"fwd": w.fwd_flops(), "bwd": w.bwd_flops(), "quant": 0.0,
+            "fwd_fp8": w.fwd_flops()}
+
+
+def component_bytes(w: wl.Workload):
+    """Algorithmic HBM bytes per launch of each component."""
+    BH, N, d = w.B * w.H, w.N, w.d
+    elems = BH * N * d
+    return {"fwd": 4 * elems * 2 + BH * N * 4,
+            "bwd": 8 * elems * 2 + BH * N * 4,
+            "quant": 3 * (elems * 2 + elems + BH * ((N + 63) // 64) * 4),
+            "fwd_fp8": 3 * elems + elems * 2 + BH * N * 4 + 3 * BH * ((N + 63) // 64) * 4}
+
+
+def available_components(attn, step_probe=None):
+    """Components whose entry points are implemented in this build."""
+    return [c for c in COMPONENTS if c in os.environ.get("ATTN_BENCH_COMPONENTS",
+                                                           ",".join(COMPONENTS)).split(",")]
+
+
+def run_gpu(args, rank, world, local_rank):
+    import exact_attention_75_gb300 as attn
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    comps = []
+    # keep only components the library implements (unsupported ones raise)
+    trial = Step(attn, w.with_(B=1, H=1, N=256), dev, COMPONENTS)
+    for c in available_components(attn):
+        try:
+            trial.run(c)
+            torch.cuda.synchronize()
+            comps.append(c)
+        except Exception as e:  # noqa: BLE001
+            if "UNSUPPORTED" not in str(e):
+                raise
+    del trial
+    st = Step(attn, w, dev, comps)
+    flops = component_flops(w)
+    nbytes = component_bytes(w)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for c in comps:
+            st.run(c)
+    torch.cuda.synchronize()
+    status = attn.poll_status()
+    if status[0] != 0:
+        raise RuntimeError(f"device status after warm-up: {status}")
+
+    ev = {c: [] for c in comps}
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        for c in comps:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            st.run(c)
+            e1.record(stream)
+            ev[c].append((e0, e1))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = t0.elapsed_time(t1)
+    per = {c: statistics.mean(a.elapsed_time(b) for a, b in ev[c]) for c in comps}
+    status = attn.poll_status()
+    if status[0] != 0:
+        raise RuntimeError(f"device status after timed region: {status}")
+
+    # e2e through the public API with host buffers: H2D of the inputs and
+    # D2H of every output inside the timed region.
+    outs = st.outputs()
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(st.host[n].numel() * st.host[n].element_size() for n in ("q", "k", "v", "do"))
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    e2e_steps = max(3, min(args.steps, 20))
+    for it in range(e2e_steps + 1):
+        if it == 1:
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for n in ("q", "k", "v", "do"):
+            getattr(st, n).copy_(st.host[n], non_blocking=True)
+        for c in comps:
+            st.run(c)
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    step_flops = sum(flops[c] for c in comps)
+    ms_step = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+    return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks,
+                flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
+                launches=sum(LAUNCHES[c] for c in comps) * args.steps)
+
+
+# ------------------------------------------------------ oracle (CPU) arm -----
+
+def cpu_oracle_sample(budget_s: float = 20.0):
+    """Time the fp64 oracle (as it stands) on one head of the workload.
+
+    Forward + backward of one (b, h) head at N = 8192, d = 128; repeated while
+    the time budget lasts.  Returns (TFLOP/s, seconds, heads done, threads).
+    """
+    import numpy as np
+    import oracle
+    w = WORKLOAD.with_(B=1, H=1)
+    inp = wl.make_inputs(w, with_do=True)
+    q, k, v, do = (inp[n][0, 0].to(torch.float64).numpy() for n in ("q", "k", "v", "do"))
+    heads = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.attention_head(q, k, v, w.causal, w.scale)
+        oracle.attention_backward_head(q, k, v, do, w.causal, w.scale)
+        heads += 1
+        if time.perf_counter() - t0 > budget_s / 2 or heads >= 8:
+            break
+    dt = time.perf_counter() - t0
+    fl = heads * (w.fwd_flops() + w.bwd_flops())
+    _ = np
+    return fl / dt / 1e12, dt, heads, os.cpu_count()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks = load_peaks()
+    w = WORKLOAD
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = []
+        for _ in range(args.warmup > 0 and 1 or 0):
+            cpu_oracle_sample(budget_s=4.0)
+        heads_total, t_total = 0, 0.0
+        for _ in range(args.steps):
+            tf, dt, heads, cores = cpu_oracle_sample(budget_s=min(20.0, 120.0 / args.steps))
+            per_step.append(tf)
+            heads_total += heads
+            t_total += dt
+        value = statistics.mean(per_step)
+        sample = (f"fwd+bwd of {heads_total} (b,h) head(s) of the workload (N=8192, d=128, "
+                  f"causal) in fp64 numpy over {args.steps} step(s)")
+        line = {"metric": "attention fwd/bwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+                "impl": "reference", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1000 * t_total / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                           "causal": w.causal},
+                "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    r = run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+
+    comps, per = r["comps"], r["per"]
+    value = world * r["step_flops"] / (r["ms_step"] * 1e-3) / 1e12
+    e2e_val = world * r["step_flops"] / (r["e2e_ms"] * 1e-3) / 1e12
+    breakdown = {}
+    for c in comps:
+        ms = per[c]
+        tf = r["flops"][c] / (ms * 1e-3) / 1e12 if r["flops"][c] else None
+        breakdown[c] = {"ms": round(ms, 4), "tflops": None if tf is None else round(tf, 1),
+                        "gbs": round(r["nbytes"][c] / (ms * 1e-3) / 1e9, 1)}
+    # dominant kernel = largest share of the step's time
+    dom = max(comps, key=lambda c: per[c])
+    if r["flops"][dom] > 0:
+        ach = r["flops"][dom] / (per[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        if dom == "fwd_fp8":
+            peak = 2 * peaks["bf16_tflops"]  # E4M3 dense = 2x bf16 (nominal ratio)
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                "peak_kind": f"{peaks['source']} bf16 burst"}
+    else:
+        ach = r["nbytes"][dom] / (per[dom] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None}
+    line = {"metric": "attention fwd/bwd TFLOP/s", "value": round(value, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(r["ms_step"], 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "components": comps,
+                       "l2": "inputs (q,k,v,dO = 256 MiB) larger than L2; no flush",
+                       "parallelism": f"replicas x{world}"},
+            "breakdown": breakdown, "roofline": roof, "clocks": r["clocks"],
+            "gpu_launches": r["launches"],
+            "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}}
+    if not args.no_cpu_baseline:
+        tf, dt, heads, cores = cpu_oracle_sample()
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"fp64 numpy fwd+bwd of {heads} head(s) "
+                                          f"(N=8192, d=128, causal), {dt:.1f} s"}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+"""GB300-native exact attention (sm_103a): Python binding of ``libattn``.
+
+Every function here only marshals arguments: it checks tensors, takes their
+device pointers and the current CUDA stream, and calls the C ABI declared in
+``include/attn.h``.  All computation runs in the library's CUDA kernels.  If
+the library has not been built, or no sm_103a GPU is present, calls raise —
+there is no fallback path.
+
+Build the library first::
+
+    python -m exact_attention_75_gb300.build
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["AttnError", "lib", "lib_path", "fwd", "bwd", "bwd_workspace_bytes", "quantize_fp8",
+           "fwd_fp8", "poll_status", "set_wait_limit_us", "selftest_wait_timeout", "num_sms",
+           "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+          3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}
+_F16, _BF16 = 0, 1
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, what: str, status: int, detail: int = 0):
+        super().__init__(f"{what} failed: {STATUS.get(status, status)} (detail 0x{detail:x})")
+        self.status = status
+        self.detail = detail
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "_build", "libattn.so")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattn.so (built in-tree) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m exact_attention_75_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    sigs = {
+        "attn_fwd": ([vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp], i),
+        "attn_bwd_workspace_bytes": ([i, i, i, i], sz),
+        "attn_bwd": ([vp] * 10 + [sz, i, i, i, i, i, f, i, vp], i),
+        "attn_quantize_fp8": ([vp, vp, vp, i, i, i, i, i, vp, i, vp], i),
+        "attn_fwd_fp8": ([vp] * 8 + [i, i, i, i, i, f, vp], i),
+        "attn_poll_device_status": ([vp, u32p], i),
+        "attn_set_wait_limit_us": ([ctypes.c_uint64], i),
+        "attn_selftest_wait_timeout": ([ctypes.c_uint64, vp, u32p], i),
+        "attn_status_string": ([i], ctypes.c_char_p),
+        "attn_num_sms": ([], i),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise AttnError(what, status)
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return _F16
+    if t.dtype == torch.bfloat16:
+        return _BF16
+    raise TypeError(f"q/k/v must be float16 or bfloat16, got {t.dtype}")
+
+
+def _check_qkv(*ts: torch.Tensor) -> Tuple[int, int, int, int]:
+    q = ts[0]
+    if q.dim() != 4:
+        raise ValueError("tensors must be [B, H, N, d]")
+    for t in ts:
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("q, k, v (and o, dO) must share shape and dtype")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, N, d]")
+    B, H, N, d = q.shape
+    return B, H, N, d
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+        scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+        lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O, LSE = attention(q, k, v).  q,k,v: [B,H,N,d] fp16/bf16, d in {64,128}."""
+    B, H, N, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_qkv(q, out)
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                            int(bool(causal)), float(scale), _dtype_code(q), _stream(q))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, H, N, d))
+
+
+def bwd(q, k, v, o, do, lse, causal: bool = False, scale: Optional[float] = None,
+        workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None):
+    """dQ, dK, dV of the loss with gradient ``do`` w.r.t. O (d = 128)."""
+    B, H, N, d = _check_qkv(q, k, v, o, do)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    with torch.cuda.device(q.device):
+        st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                            _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H, N, d,
+                            int(bool(causal)), float(scale), _dtype_code(q), _stream(q))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def quantize_fp8(x: torch.Tensor, signs: Optional[torch.Tensor] = None,
+                 transposed: bool = False, block_rows: int = 64):
+    """E4M3 codes (uint8) and per-64-row fp32 scales of a bf16 [B,H,N,d] tensor.
+
+    ``signs``: optional int8 CUDA tensor of d values +-1 (randomized Hadamard).
+    ``transposed``: write the codes as [B,H,d,N] (the layout attn_fwd_fp8 wants
+    for V).
+    """
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.dim() != 4:
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [B,H,N,d]")
+    B, H, N, d = x.shape
+    codes = torch.empty((B, H, d, N) if transposed else (B, H, N, d), dtype=torch.uint8,
+                        device=x.device)
+    scales = torch.empty((B, H, (N + block_rows - 1) // block_rows), dtype=torch.float32,
+                         device=x.device)
+    if signs is not None:
+        if signs.dtype != torch.int8 or not signs.is_cuda or signs.numel() != d:
+            raise ValueError("signs must be an int8 CUDA tensor of d values")
+    with torch.cuda.device(x.device):
+        st = lib().attn_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B, H, N, d, block_rows,
+                                     _ptr(signs), int(bool(transposed)), _stream(x))
+    _check(st, "attn_quantize_fp8")
+    return codes, scales
+
+
+def fwd_fp8(q8, k8, v8t, q_scale, k_scale, v_scale, causal: bool = False,
+            scale: Optional[float] = None, out=None, lse=None):
+    """FP8 forward: E4M3 q8, k8 [B,H,N,d], v8t [B,H,d,N] + block scales -> bf16 O, fp32 LSE."""
+    B, H, N, d = q8.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (q8, k8, v8t, q_scale, k_scale, v_scale):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    with torch.cuda.device(q8.device):
+        st = lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(q_scale), _ptr(k_scale),
+                                _ptr(v_scale), _ptr(out), _ptr(lse), B, H, N, d,
+                                int(bool(causal)), float(scale), _stream(q8))
+    _check(st, "attn_fwd_fp8")
+    return out, lse
+
+
+def poll_status(device=None) -> Tuple[int, int]:
+    """Synchronise the current stream and read/clear the device status word."""
+    detail = ctypes.c_uint32(0)
+    s = torch.cuda.current_stream(device)
+    st = lib().attn_poll_device_status(ctypes.c_void_p(s.cuda_stream), ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def set_wait_limit_us(us: int) -> None:
+    _check(lib().attn_set_wait_limit_us(int(us)), "attn_set_wait_limit_us")
+
+
+def selftest_wait_timeout(limit_us: int = 20000, device=None) -> Tuple[int, int]:
+    detail = ctypes.c_uint32(0)
+    s = torch.cuda.current_stream(device)
+    st = lib().attn_selftest_wait_timeout(int(limit_us), ctypes.c_void_p(s.cuda_stream),
+                                          ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def num_sms() -> int:
+    return int(lib().attn_num_sms())

@@ -1,0 +1,366 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// TMA descriptor construction, launch configuration and the device status
+// word.  No function here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "bwd.cuh"
+#include "fp8.cuh"
+#include "fwd.cuh"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+// Status word written by kernels whose pipeline waits ran out of time.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  bool supported = false;
+  uint32_t* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+attn_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    di.supported = (major == 10 && minor == 3);
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
+    di.status = static_cast<uint32_t*>(addr);
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    di.ready = true;
+  }
+  if (!di.supported) return ATTN_ERR_UNSUPPORTED;
+  *out = &di;
+  return ATTN_OK;
+}
+
+attn_status launch_result(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  if (e == cudaErrorNotSupported) {
+    cudaGetLastError();
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  return ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// 3-D tiled map over a contiguous [outer, rows, inner] tensor with the
+// 128-byte swizzle; box = [1, box_rows, box_inner].
+bool encode_3d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esize, int64_t inner,
+               int64_t rows, int64_t outer, int box_inner, int box_rows,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)(inner * esize), (cuuint64_t)(inner * rows * esize)};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool shape_ok(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return false;
+  if (d != 64 && d != 128) return false;
+  const int64_t bh = (int64_t)B * H;
+  if (bh > (1 << 30) || N > (1 << 28)) return false;
+  return bh * N * d < (int64_t)1 << 40;
+}
+
+}  // namespace
+
+attn_status fill_fwd_common(FwdLaunch* a, DeviceInfo* di, int B, int H, int N, float scale,
+                            void* stream, void* o, float* lse) {
+  FwdParams& p = a->params;
+  p.o = o;
+  p.lse = lse;
+  p.status = di->status;
+  p.BH = B * H;
+  p.N = N;
+  p.n_qtiles = (N + 127) / 128;
+  p.n_pairs = (p.n_qtiles + 1) / 2;
+  p.n_kblocks = (N + 127) / 128;
+  p.num_units = p.BH * p.n_pairs;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a->num_ctas = di->num_sms;
+  a->stream = static_cast<cudaStream_t>(stream);
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+int attn_num_sms(void) {
+  DeviceInfo* di = nullptr;
+  if (device_info(&di) != ATTN_OK) return 0;
+  return di->num_sms;
+}
+
+attn_status attn_set_wait_limit_us(uint64_t limit_us) {
+  if (limit_us > 3600ull * 1000000ull) return ATTN_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(limit_us == 0 ? kDefaultWaitNs : limit_us * 1000ull);
+  return ATTN_OK;
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, int causal, float scale, attn_dtype dtype,
+                     void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  attn_status st = device_info(&di);
+  if (st != ATTN_OK) return st;
+  FwdLaunch a;
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int64_t BH = (int64_t)B * H;
+  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmK, k, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, BH, 64, 128))
+    return ATTN_ERR_CUDA;
+  fill_fwd_common(&a, di, B, H, N, scale, stream, o, lse);
+  cudaError_t e = launch_fwd(a, d, causal != 0, dtype == ATTN_BF16);
+  return launch_result(e);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (!shape_ok(B, H, N, d)) return 0;
+  const size_t rows = (size_t)B * H * N;
+  const size_t dbytes = (rows * 4 + 255) & ~(size_t)255;
+  const size_t qbytes = (rows * d * 4 + 255) & ~(size_t)255;
+  return dbytes + qbytes;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                     int causal, float scale, attn_dtype dtype, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  attn_status st = device_info(&di);
+  if (st != ATTN_OK) return st;
+  BwdLaunch a;
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int64_t BH = (int64_t)B * H;
+  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmK, k, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmDO, dout, dt, 2, d, N, BH, 64, 128))
+    return ATTN_ERR_CUDA;
+  const size_t rows = (size_t)BH * N;
+  const size_t dbytes = (rows * 4 + 255) & ~(size_t)255;
+  BwdParams& p = a.params;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.delta = static_cast<float*>(workspace);
+  p.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dbytes);
+  p.status = di->status;
+  p.BH = (int)BH;
+  p.N = N;
+  p.n_qtiles = (N + 127) / 128;
+  p.n_kblocks = (N + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a.num_sms = di->num_sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.causal = causal != 0;
+  a.bf16 = dtype == ATTN_BF16;
+  cudaError_t e = launch_bwd(a);
+  return launch_result(e);
+}
+
+attn_status attn_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales, int B, int H,
+                              int N, int d, int block_rows, const int8_t* hadamard_signs,
+                              int write_transposed, void* stream) {
+  if (!aligned16(x_bf16) || !aligned16(x_e4m3) || scales == nullptr ||
+      (reinterpret_cast<uintptr_t>(scales) & 3) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (block_rows != 64) return ATTN_ERR_UNSUPPORTED;
+  if (write_transposed != 0 && write_transposed != 1) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  if (write_transposed && (N % 16) != 0) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  attn_status st = device_info(&di);
+  if (st != ATTN_OK) return st;
+  QuantLaunch a;
+  a.x = x_bf16;
+  a.out = x_e4m3;
+  a.scales = scales;
+  a.signs = hadamard_signs;
+  a.BH = B * H;
+  a.N = N;
+  a.d = d;
+  a.transposed = write_transposed != 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_quantize(a);
+  return launch_result(e);
+}
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                         const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                         int H, int N, int d, int causal, float scale, void* stream) {
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  if (q_scale == nullptr || k_scale == nullptr || v_scale == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!shape_ok(B, H, N, d) || (N % 16) != 0) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  attn_status st = device_info(&di);
+  if (st != ATTN_OK) return st;
+  Fp8FwdLaunch a;
+  const int64_t BH = (int64_t)B * H;
+  if (!encode_3d(&a.tmQ, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128, 128) ||
+      !encode_3d(&a.tmK, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, d, N, BH, 128, 128) ||
+      !encode_3d(&a.tmVt, v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, d, BH, 128, 128))
+    return ATTN_ERR_CUDA;
+  fill_fwd_common(&a.base, di, B, H, N, scale, stream, o, lse);
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.causal = causal != 0;
+  cudaError_t e = launch_fwd_fp8(a);
+  return launch_result(e);
+}
+
+attn_status attn_poll_device_status(void* stream, uint32_t* detail) {
+  DeviceInfo* di = nullptr;
+  attn_status st = device_info(&di);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, di->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (detail != nullptr) *detail = word;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return (word & 0xFF) == kStatusTimeout ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"
+
+namespace attn {
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives at; the bounded wait
+// must give up, record the timeout and return.
+__global__ void selftest_wait_kernel(uint32_t* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Watchdog wd{status, &abort_flag, limit_ns};
+    mbar_wait(smem_u32(&bar), 0, wd, 99);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" attn_status attn_selftest_wait_timeout(uint64_t limit_us, void* stream,
+                                                  uint32_t* detail) {
+  if (limit_us == 0 || limit_us > 10ull * 1000000ull) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  attn_status st = device_info(&di);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selftest_wait_kernel<<<1, 32, 0, s>>>(di->status, limit_us * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  return attn_poll_device_status(stream, detail);
+}

@@ -1,0 +1,41 @@
+// Host <-> device interface of the backward kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace attn {
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;      // [B*H, N] natural-log LSE from the forward pass
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;          // workspace: D_i = sum_c dO_ic O_ic  [B*H, N]
+  float* dq_acc;         // workspace: fp32 dQ accumulator     [B*H, N, D]
+  uint32_t* status;
+  int BH, N;
+  int n_qtiles;          // ceil(N / 128)
+  int n_kblocks;         // ceil(N / 128)
+  float scale;
+  float scale_log2;      // scale * log2(e)
+  unsigned long long wait_limit_ns;
+};
+
+struct BwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmDO;
+  BwdParams params;
+  int num_sms;
+  cudaStream_t stream;
+  bool causal, bf16;
+};
+
+cudaError_t launch_bwd(const BwdLaunch& a);
+
+}  // namespace attn

@@ -1,0 +1,456 @@
+// Forward pass of exact attention on sm_103a: TMA-fed, tcgen05 tensor cores
+// with S and O accumulated in tensor memory, online softmax in base 2.
+//
+// Algorithm: "FlashAttention-2: Faster Attention with Better Parallelism and
+// Work Partitioning" (review page), flowchart "프레임워크 개요": per query
+// tile, loop over K/V tiles computing S = Q K^T and the running row max /
+// row sum, accumulate P V unnormalised, rescale by 1/rowsum once at the end,
+// write O and the log-sum-exp ("Methods"); blocks entirely above the causal
+// diagonal are never visited ("핵심 구성요소").  The exp2 formulation with the
+// scale folded into the exponent is the one "Triton 07: Flash Attention v3"
+// ("Method") keeps from its FA2 core.
+//
+// CTA organisation (one CTA per SM, persistent):
+//   warps 0-3  softmax warpgroup for query tile 0 of the current work unit
+//   warps 4-7  softmax warpgroup for query tile 1
+//   warp  8    TMA producer: Q tiles, then a ring of K and V tiles
+//   warp  9    tcgen05 issuer (one thread) + tensor-memory owner
+// A work unit is (batch*head, pair of adjacent 128-row query tiles).  The two
+// tiles share every K/V tile and ping-pong on the tensor core: while one
+// warpgroup exponentiates S_t, the tensor core computes the other tile's
+// P V and next S ("8.3 FlashAttention-3", section 4, pingpong scheduling,
+// recast for an MMA warp that issues for both tiles).
+//
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   [  0,128) S_0 (fp32); P_0 (16-bit, packed in pairs) overwrites [0,64)
+//   [128,256) S_1 / P_1
+//   [256,256+D) O_0 (fp32)     [256+D,256+2D) O_1
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "fwd.cuh"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kTileBytes = 128 * D * 2;       // 128 rows x D 16-bit values
+  static constexpr int kSlots = (D == 128) ? 4 : 8;    // K/V ring depth (tiles)
+  static constexpr int kQOff = 0;
+  static constexpr int kKvOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKvOff + kSlots * kTileBytes;
+  // barrier indices
+  static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8, kDrain = 10;
+  static constexpr int kKvFull = 11, kKvEmpty = 11 + kSlots;
+  static constexpr int kNumBars = 11 + 2 * kSlots;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kDynSmem = kBytes + 1024;  // + alignment slack
+  static_assert(kDynSmem <= 232448, "shared memory budget (227 KB) exceeded");
+};
+
+struct Unit {
+  int bh, qp;
+  int nb[2];  // K/V blocks visited by query tile 0 / 1 (0 = tile absent)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
+  Unit w;
+  if (CAUSAL) {
+    // Longest first: the heaviest query-tile pairs of every head come first.
+    const int r = u / p.BH;
+    w.bh = u - r * p.BH;
+    w.qp = p.n_pairs - 1 - r;
+  } else {
+    w.bh = u / p.n_pairs;
+    w.qp = u - w.bh * p.n_pairs;
+  }
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int tile = 2 * w.qp + t;
+    if (tile >= p.n_qtiles) {
+      w.nb[t] = 0;
+    } else {
+      w.nb[t] = CAUSAL ? min(tile + 1, p.n_kblocks) : p.n_kblocks;
+    }
+  }
+  return w;
+}
+
+// Snake order over the persistent grid: round k gives CTA c the unit
+// k*G + c (k even) or k*G + G-1-c (k odd), which evens out the
+// longest-first costs across CTAs.
+__device__ __forceinline__ int unit_of(int k, int cta, int G) {
+  return k * G + ((k & 1) ? (G - 1 - cta) : cta);
+}
+
+template <int D>
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int k16) {
+  // K-major 16-bit tile stored as D/64 swizzle-128B column halves of
+  // [128 rows][64 values]; step k16 selects 16 values of the reduction dim.
+  const uint32_t addr = tile_addr + (uint32_t)(k16 >> 2) * 16384u + (uint32_t)(k16 & 3) * 32u;
+  return sdesc_sw128(addr, 16, 1024);
+}
+
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_addr, int k16) {
+  // V tile as the MN-major B operand (N = head dim, contiguous): 8-row groups
+  // of keys are 1024 B apart (SBO), 64-value column halves 16 KB apart (LBO).
+  return sdesc_sw128(tile_addr + (uint32_t)k16 * 2048u, 16384, 1024);
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::kBarOff;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  Watchdog wd{p.status, abort_flag, p.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::kQFull + t), 1);
+      mbar_init(bar(L::kQEmpty + t), 1);
+      mbar_init(bar(L::kSFull + t), 1);
+      mbar_init(bar(L::kPFull + t), 128);
+      mbar_init(bar(L::kOFull + t), 1);
+    }
+    mbar_init(bar(L::kDrain), 1);
+    for (int s = 0; s < L::kSlots; ++s) {
+      mbar_init(bar(L::kKvFull + s), 1);
+      mbar_init(bar(L::kKvEmpty + s), 1);
+    }
+    mbar_fence_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------ TMA producer ---
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t kv_it = 0, q_it[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = unit_of(k, cta, G);
+        if (u >= p.num_units) break;
+        const Unit w = decode_unit<CAUSAL>(u, p);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (w.nb[t] == 0) continue;
+          ok = mbar_wait(bar(L::kQEmpty + t), (q_it[t] & 1) ^ 1, wd, 1);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
+          const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(dst + h * 16384, &tmQ, bar(L::kQFull + t), h * 64,
+                        (2 * w.qp + t) * 128, w.bh);
+          ++q_it[t];
+        }
+        const int nbmax = max(w.nb[0], w.nb[1]);
+        for (int j = 0; j < nbmax && ok; ++j) {
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t slot = kv_it % L::kSlots;
+            ok = mbar_wait(bar(L::kKvEmpty + slot), ((kv_it / L::kSlots) & 1) ^ 1, wd, 2);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(L::kKvFull + slot), L::kTileBytes);
+            const uint32_t dst = sbase + L::kKvOff + slot * L::kTileBytes;
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(dst + h * 16384, which ? &tmV : &tmK, bar(L::kKvFull + slot), h * 64,
+                          j * 128, w.bh);
+            ++kv_it;
+          }
+        }
+      }
+      // Drain: every copy this warp issued must have landed before the CTA
+      // may exit (only matters after an abort; otherwise all were consumed).
+      Watchdog dw = wd;
+      volatile int never = 0;
+      dw.abort_flag = &never;
+      const uint32_t first = kv_it > (uint32_t)L::kSlots ? kv_it - L::kSlots : 0u;
+      for (uint32_t it = first; it < kv_it; ++it)
+        mbar_wait(bar(L::kKvFull + it % L::kSlots), (it / L::kSlots) & 1, dw, 3);
+      for (int t = 0; t < 2; ++t)
+        if (q_it[t] > 0) mbar_wait(bar(L::kQFull + t), (q_it[t] - 1) & 1, dw, 4);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------- tcgen05 issuer ---
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t kIdO = idesc_f16(128, D, BF16, false, true);
+      uint32_t kv_it = 0, q_it[2] = {0, 0}, p_it[2] = {0, 0};
+      bool ok = true;
+      const uint32_t qaddr[2] = {sbase + L::kQOff, sbase + L::kQOff + L::kTileBytes};
+      for (int k = 0; ok; ++k) {
+        const int u = unit_of(k, cta, G);
+        if (u >= p.num_units) break;
+        const Unit w = decode_unit<CAUSAL>(u, p);
+        const int nbmax = max(w.nb[0], w.nb[1]);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (w.nb[t] == 0) continue;
+          ok = mbar_wait(bar(L::kQFull + t), q_it[t] & 1, wd, 5);
+          ++q_it[t];
+        }
+        if (!ok) break;
+        // S_t(0) = Q_t K_0^T for both tiles.
+        uint32_t kslot = kv_it % L::kSlots;
+        ok = mbar_wait(bar(L::kKvFull + kslot), (kv_it / L::kSlots) & 1, wd, 6);
+        if (!ok) break;
+        ++kv_it;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (w.nb[t] == 0) continue;
+          const uint32_t kaddr = sbase + L::kKvOff + kslot * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16_ss(tbase + 128 * t, kmajor_desc<D>(qaddr[t], kk), kmajor_desc<D>(kaddr, kk),
+                       kIdS, kk > 0);
+          mma_commit(bar(L::kSFull + t));
+          if (w.nb[t] == 1) mma_commit(bar(L::kQEmpty + t));
+        }
+        mma_commit(bar(L::kKvEmpty + kslot));
+        for (int j = 0; j < nbmax && ok; ++j) {
+          const uint32_t vslot = kv_it % L::kSlots;
+          ok = mbar_wait(bar(L::kKvFull + vslot), (kv_it / L::kSlots) & 1, wd, 7);
+          if (!ok) break;
+          ++kv_it;
+          const bool have_next = j + 1 < nbmax;
+          if (have_next) {
+            kslot = kv_it % L::kSlots;
+            ok = mbar_wait(bar(L::kKvFull + kslot), (kv_it / L::kSlots) & 1, wd, 8);
+            if (!ok) break;
+            ++kv_it;
+          }
+          const uint32_t vaddr = sbase + L::kKvOff + vslot * L::kTileBytes;
+          const uint32_t kaddr = sbase + L::kKvOff + kslot * L::kTileBytes;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= w.nb[t]) continue;
+            ok = mbar_wait(bar(L::kPFull + t), p_it[t] & 1, wd, 9);
+            if (!ok) break;
+            ++p_it[t];
+            tc_fence_after();
+            // O_t += P_t V_j  (A = P from tensor memory, 16 keys per MMA)
+            const uint32_t ocol = tbase + 256 + D * t;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ts(ocol, tbase + 128 * t + kk * 8, mnmajor_desc(vaddr, kk), kIdO,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+            if (j == w.nb[t] - 1) mma_commit(bar(L::kOFull + t));
+            if (j + 1 < w.nb[t]) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_f16_ss(tbase + 128 * t, kmajor_desc<D>(qaddr[t], kk),
+                           kmajor_desc<D>(kaddr, kk), kIdS, kk > 0);
+              mma_commit(bar(L::kSFull + t));
+              if (j + 1 == w.nb[t] - 1) mma_commit(bar(L::kQEmpty + t));
+            }
+          }
+          if (!ok) break;
+          mma_commit(bar(L::kKvEmpty + vslot));
+          if (have_next) mma_commit(bar(L::kKvEmpty + kslot));
+        }
+      }
+      // Drain: wait until every MMA issued above has completed.
+      mma_commit(bar(L::kDrain));
+      Watchdog dw = wd;
+      volatile int never = 0;
+      dw.abort_flag = &never;
+      mbar_wait(bar(L::kDrain), 0, dw, 10);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------- softmax warpgroups ---
+    const int t = warp >> 2;                 // query tile of the pair
+    const int r = threadIdx.x & 127;         // row within the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tbase + lane_base + 128u * t;
+    const uint32_t o_addr = tbase + lane_base + 256u + D * t;
+    const float sl2 = p.scale_log2;
+    uint32_t s_it = 0, o_it = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int u = unit_of(k, cta, G);
+      if (u >= p.num_units) break;
+      const Unit w = decode_unit<CAUSAL>(u, p);
+      const int nb = w.nb[t];
+      if (nb == 0) continue;
+      const int tile = 2 * w.qp + t;
+      const int row = tile * 128 + r;
+      float m = -INFINITY;  // running max of scale*log2(e)*s (reference value)
+      float l = 0.f;        // running sum of exp2(x - m)
+      for (int j = 0; j < nb; ++j) {
+        ok = mbar_wait(bar(L::kSFull + t), s_it & 1, wd, 11);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++s_it;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+        const bool diag = CAUSAL && (j == tile);
+        const bool tail = (j == p.n_kblocks - 1) && (p.N & 127);
+        if (diag || tail) {
+          const int kbase = j * 128;
+          const int lim = CAUSAL ? min(row, p.N - 1) : (p.N - 1);
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_blk = mx * sl2;
+        if (j == 0) {
+          m = m_blk;
+        } else {
+          const bool need = m_blk > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            // Raise the reference max and rescale this row of O and l.  The
+            // previous P V has completed: its MMA was issued before the S
+            // whose completion we just waited for.
+            const float m_new = need ? m_blk : m;
+            const float alpha = ex2_approx(m - m_new);
+            l *= alpha;
+            m = m_new;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t raw[32];
+              tmem_ld32_sync(o_addr + c * 32, raw);
+              uint32_t lo[16], hi[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                lo[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
+                hi[i] = __float_as_uint(__uint_as_float(raw[16 + i]) * alpha);
+              }
+              tmem_st16(o_addr + c * 32, lo);
+              tmem_st16(o_addr + c * 32 + 16, hi);
+            }
+          }
+        }
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        float rowsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
+            const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
+            rowsum += p0 + p1;
+            pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+          }
+          tmem_st16(s_addr + c * 16, pk);
+        }
+        l += rowsum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::kPFull + t));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------- epilogue ---
+      ok = mbar_wait(bar(L::kOFull + t), o_it & 1, wd, 12);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ++o_it;
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const size_t grow = (size_t)w.bh * p.N + row;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld32_sync(o_addr + c * 32, raw);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = __uint_as_float(raw[2 * i]) * inv_l;
+          const float b = __uint_as_float(raw[2 * i + 1]) * inv_l;
+          pk[i] = BF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+        }
+        if (row < p.N) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            orow[c * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (row < p.N) p.lse[grow] = (m + log2f(l)) * 0.69314718055994530942f;
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_one(const FwdLaunch& a) {
+  using L = FwdLayout<D>;
+  auto kern = fwd_kernel<D, CAUSAL, BF16>;
+  static bool configured = false;  // attribute set once per instantiation
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = a.params.num_units < a.num_ctas ? a.params.num_units : a.num_ctas;
+  kern<<<grid, kThreads, L::kDynSmem, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.params);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdLaunch& a, int d, bool causal, bool bf16) {
+  if (d == 128) {
+    if (causal) return bf16 ? launch_one<128, true, true>(a) : launch_one<128, true, false>(a);
+    return bf16 ? launch_one<128, false, true>(a) : launch_one<128, false, false>(a);
+  }
+  if (causal) return bf16 ? launch_one<64, true, true>(a) : launch_one<64, true, false>(a);
+  return bf16 ? launch_one<64, false, true>(a) : launch_one<64, false, false>(a);
+}
+
+}  // namespace attn

@@ -1,0 +1,32 @@
+// Host <-> device interface of the forward kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace attn {
+
+struct FwdParams {
+  void* o;              // [B*H, N, D] 16-bit output
+  float* lse;           // [B*H, N] fp32 output
+  uint32_t* status;     // device status word
+  int BH, N;
+  int n_qtiles;         // ceil(N / 128)
+  int n_pairs;          // ceil(n_qtiles / 2): work units per head
+  int n_kblocks;        // ceil(N / 128)
+  int num_units;        // BH * n_pairs
+  float scale_log2;     // scale * log2(e)
+  unsigned long long wait_limit_ns;
+};
+
+struct FwdLaunch {
+  CUtensorMap tmQ, tmK, tmV;
+  FwdParams params;
+  int num_ctas;         // persistent grid size (number of SMs)
+  cudaStream_t stream;
+};
+
+cudaError_t launch_fwd(const FwdLaunch& a, int d, bool causal, bool bf16);
+
+}  // namespace attn

@@ -1,0 +1,167 @@
+/*
+ * attn.h — C ABI of libattn: exact scaled-dot-product attention on one
+ * NVIDIA GB300 (sm_103a), computed in tiles with an online softmax.
+ *
+ * The operation is the one described by "FlashAttention-2: Faster Attention
+ * with Better Parallelism and Work Partitioning" (paper review page): the
+ * flowchart under "프레임워크 개요" (Q, K, V in HBM; per (batch, head,
+ * query-block) thread block; load the Q tile; iterate over K/V tiles with
+ * QK^T and online-softmax statistics; accumulate softmax(S) V; rescale once at
+ * the end; write O and the log-sum-exp), its "Methods" section (deferred
+ * 1/rowsum scaling, only the log-sum-exp is stored and reused by the
+ * backward pass) and "핵심 구성요소" (blocks entirely above the causal
+ * diagonal are skipped; the backward pass recomputes with the stored
+ * log-sum-exp).  The FP8 entry points follow "8.3 FlashAttention-3",
+ * sections 5.1 (block quantization) and 5.2 (incoherent processing with a
+ * Hadamard transform).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout: Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d] row-major and
+ *    contiguous (d innermost); LSE and the delta vector D are [B, H, N].
+ *    All pointers are DEVICE pointers, 16-byte aligned (TMA requirement).
+ *  - Shapes: d in {64, 128}; N >= 1 (any N: partial tiles are zero-filled
+ *    on load and masked); B, H >= 1; B*H*N*d must fit in 2^31 elements.
+ *  - Causal masking is top-left aligned: key j is visible to query i iff
+ *    j <= i.  `scale` multiplies QK^T (1/sqrt(d) in the usual case).
+ *  - LSE is the natural log of sum_j exp(scale * q_i . k_j) over the visible
+ *    keys, stored as fp32.
+ *  - Ownership: the caller allocates and owns all memory.  No entry point
+ *    allocates device memory; the backward pass takes a caller-provided
+ *    workspace (see attn_bwd_workspace_bytes).
+ *  - Asynchrony: every compute call is enqueued on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and returns ATTN_OK once the launches
+ *    are accepted.  Kernel-side failures (a pipeline wait that ran out of
+ *    time) are reported later by attn_poll_device_status.
+ *  - Errors: invalid arguments return ATTN_ERR_INVALID_ARG / _UNSUPPORTED
+ *    before anything is launched; no exception crosses the ABI.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or flag */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid but unsupported (d, dtype, device)  */
+  ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed          */
+  ATTN_ERR_TIMEOUT = 4       /* a kernel pipeline wait ran out of time     */
+} attn_status;
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * Forward pass.  O = softmax(scale * Q K^T, masked) V and
+ * LSE_i = log sum_j exp(scale * q_i . k_j).
+ *   q, k, v : [B,H,N,d] fp16 or bf16 (per `dtype`), read only.
+ *   o       : [B,H,N,d] same dtype, written (round to nearest even).
+ *   lse     : [B,H,N] fp32, written.
+ *   causal  : 0 or 1.
+ * Cite: FlashAttention-2 review, flowchart "프레임워크 개요" and "Methods";
+ * causal block skipping in "핵심 구성요소".
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, int causal, float scale, attn_dtype dtype,
+                     void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs: the delta vector
+ * D_i = sum_c dO_ic O_ic (fp32 [B,H,N]) and the fp32 dQ accumulator
+ * ([B,H,N,d]), each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass for the loss whose gradient with respect to O is `dout`.
+ * Recomputes P from `lse` (written by attn_fwd on the same inputs) and writes
+ *   dV = P^T dO,  dS = P o (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, k, v, o, dout : [B,H,N,d] fp16/bf16, read only.
+ *   lse              : [B,H,N] fp32 from attn_fwd, read only.
+ *   dq, dk, dv       : [B,H,N,d] same dtype, written.
+ *   workspace        : >= attn_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte
+ *                      aligned, caller-owned; contents on entry are ignored
+ *                      and on return are unspecified.
+ * Only d = 128 is supported by the backward kernels (ATTN_ERR_UNSUPPORTED
+ * otherwise).  dQ is accumulated in fp32 with atomic adds, so its last bits
+ * may vary from run to run.
+ * Cite: FlashAttention-2 review, "Methods" (log-sum-exp kept for the backward
+ * pass) and "핵심 구성요소" (backward recomputation with the log-sum-exp).
+ */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                     int causal, float scale, attn_dtype dtype, void* stream);
+
+/*
+ * FP8 E4M3 block quantization of one bf16 tensor, optionally after the
+ * randomized Hadamard rotation x <- x H_d diag(signs) / sqrt(d).
+ *   x_bf16  : [B,H,N,d] bf16, read only.
+ *   x_e4m3  : [B,H,N,d] bytes (E4M3) — or [B,H,d,N] when write_transposed=1.
+ *   scales  : [B,H,ceil(N/block_rows)] fp32: s = amax/448 over each block of
+ *             `block_rows` rows x d columns (s = 1 if the block is all zero);
+ *             codes are E4M3(x/s), round to nearest even, saturating.
+ *   block_rows : 64 (the only supported value).
+ *   hadamard_signs : NULL (no rotation) or a DEVICE array of d int8 values,
+ *             each +1 or -1.
+ *   write_transposed : 0 or 1; 1 requires N % 16 == 0.
+ * Cite: "8.3 FlashAttention-3", sections 5.1 and 5.2.
+ */
+attn_status attn_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales, int B, int H,
+                              int N, int d, int block_rows, const int8_t* hadamard_signs,
+                              int write_transposed, void* stream);
+
+/*
+ * FP8 forward pass: O = softmax(scale * Q K^T) V with E4M3 inputs and fp32
+ * accumulation; S_ij = q8_i . k8_j * sq(i/64) * sk(j/64).
+ *   q8, k8  : [B,H,N,d] E4M3 from attn_quantize_fp8 (same rotation for both).
+ *   v8t     : [B,H,d,N] E4M3 (attn_quantize_fp8 with write_transposed=1).
+ *   q_scale, k_scale, v_scale : [B,H,ceil(N/64)] fp32 block scales.
+ *   o       : [B,H,N,d] bf16, written.   lse : [B,H,N] fp32, written.
+ * Requires d = 128 and N % 16 == 0.
+ * Cite: "8.3 FlashAttention-3", section 5 and section 6.2.
+ */
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                         const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                         int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the library's device status
+ * word.  Returns ATTN_ERR_TIMEOUT if a kernel pipeline wait ran out of time
+ * since the last poll (the kernel then skipped the rest of its work and
+ * released its resources; outputs are incomplete), ATTN_ERR_CUDA if the
+ * synchronisation failed, else ATTN_OK.  `detail` (may be NULL) receives the
+ * raw status word: code | wait-site << 8 | block index << 16.
+ */
+attn_status attn_poll_device_status(void* stream, uint32_t* detail);
+
+/*
+ * Set the time limit of every bounded pipeline wait in later launches, in
+ * microseconds (default 2,000,000 = 2 s; 0 restores the default).
+ */
+attn_status attn_set_wait_limit_us(uint64_t limit_us);
+
+/*
+ * Self-test of the failure path: launches one block that waits on an
+ * mbarrier nothing will ever arrive at, with a `limit_us` time limit.  The
+ * kernel must give up, record ATTN_ERR_TIMEOUT in the status word and exit
+ * normally.  Returns the result of attn_poll_device_status.
+ */
+attn_status attn_selftest_wait_timeout(uint64_t limit_us, void* stream, uint32_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+const char* attn_status_string(attn_status s);
+
+/* Number of SMs the persistent kernels size their grid by (device 0 current). */
+int attn_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -26,3 +26,13 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def attn_lib():
+    """The built CUDA library (built in-tree first if needed)."""
+    from exact_attention_75_gb300 import build
+    build.build()
+    import exact_attention_75_gb300 as attn
+    attn.lib()
+    return attn
