@@ -31,6 +31,7 @@
 
 #include "fwd.cuh"
 #include "sm103_ptx.cuh"
+#include "tiles.cuh"
 
 namespace attn {
 
@@ -87,27 +88,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   return w;
 }
 
-// Snake order over the persistent grid: round k gives CTA c the unit
-// k*G + c (k even) or k*G + G-1-c (k odd), which evens out the
-// longest-first costs across CTAs.
-__device__ __forceinline__ int unit_of(int k, int cta, int G) {
-  return k * G + ((k & 1) ? (G - 1 - cta) : cta);
-}
-
-template <int D>
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int k16) {
-  // K-major 16-bit tile stored as D/64 swizzle-128B column halves of
-  // [128 rows][64 values]; step k16 selects 16 values of the reduction dim.
-  const uint32_t addr = tile_addr + (uint32_t)(k16 >> 2) * 16384u + (uint32_t)(k16 & 3) * 32u;
-  return sdesc_sw128(addr, 16, 1024);
-}
-
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile_addr, int k16) {
-  // V tile as the MN-major B operand (N = head dim, contiguous): 8-row groups
-  // of keys are 1024 B apart (SBO), 64-value column halves 16 KB apart (LBO).
-  return sdesc_sw128(tile_addr + (uint32_t)k16 * 2048u, 16384, 1024);
-}
-
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -162,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_it = 0, q_it[2] = {0, 0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, cta, G);
+        const int u = snake_unit(k, cta, G);
         if (u >= p.num_units) break;
         const Unit w = decode_unit<CAUSAL>(u, p);
         for (int t = 0; t < 2 && ok; ++t) {
@@ -215,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t qaddr[2] = {sbase + L::kQOff, sbase + L::kQOff + L::kTileBytes};
       for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, cta, G);
+        const int u = snake_unit(k, cta, G);
         if (u >= p.num_units) break;
         const Unit w = decode_unit<CAUSAL>(u, p);
         const int nbmax = max(w.nb[0], w.nb[1]);
@@ -236,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kaddr = sbase + L::kKvOff + kslot * L::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_f16_ss(tbase + 128 * t, kmajor_desc<D>(qaddr[t], kk), kmajor_desc<D>(kaddr, kk),
+            mma_f16_ss(tbase + 128 * t, kmajor_desc16(qaddr[t], kk), kmajor_desc16(kaddr, kk),
                        kIdS, kk > 0);
           mma_commit(bar(L::kSFull + t));
           if (w.nb[t] == 1) mma_commit(bar(L::kQEmpty + t));
@@ -266,14 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ocol = tbase + 256 + D * t;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ts(ocol, tbase + 128 * t + kk * 8, mnmajor_desc(vaddr, kk), kIdO,
+              mma_f16_ts(ocol, tbase + 128 * t + kk * 8, mnmajor_desc16(vaddr, kk), kIdO,
                          (j > 0 || kk > 0) ? 1u : 0u);
             if (j == w.nb[t] - 1) mma_commit(bar(L::kOFull + t));
             if (j + 1 < w.nb[t]) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk)
-                mma_f16_ss(tbase + 128 * t, kmajor_desc<D>(qaddr[t], kk),
-                           kmajor_desc<D>(kaddr, kk), kIdS, kk > 0);
+                mma_f16_ss(tbase + 128 * t, kmajor_desc16(qaddr[t], kk),
+                           kmajor_desc16(kaddr, kk), kIdS, kk > 0);
               mma_commit(bar(L::kSFull + t));
               if (j + 1 == w.nb[t] - 1) mma_commit(bar(L::kQEmpty + t));
             }
@@ -302,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_it = 0, o_it = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int u = unit_of(k, cta, G);
+      const int u = snake_unit(k, cta, G);
       if (u >= p.num_units) break;
       const Unit w = decode_unit<CAUSAL>(u, p);
       const int nb = w.nb[t];

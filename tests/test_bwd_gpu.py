@@ -1,0 +1,102 @@
+"""Backward parity: CUDA path (through the C ABI) vs the fp64 oracle.
+
+O and LSE come from the library's own forward pass on the same inputs (as in
+the bf16 backward workload).  Tolerance, per gradient g in {dQ, dK, dV}:
+max |g - g_ref| <= 5e-2 * max |g_ref|.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import sample_heads, to64
+
+pytestmark = pytest.mark.gpu
+REL_TOL = 5e-2
+
+
+def _gpu_grads(attn, inp, w):
+    dev = torch.device("cuda")
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = attn.fwd(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    attn.bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv)
+    st, detail = attn.poll_status()
+    assert st == 0, f"device status {st} detail 0x{detail:x}"
+    return dq, dk, dv
+
+
+def _check(w, grads, refs, heads=None):
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, refs):
+        g = to64(g)
+        assert np.isfinite(g).all(), name
+        if heads is not None:
+            g = np.stack([g[b, h] for b, h in heads])
+            r = np.stack([r[b, h] for b, h in heads])
+        err = np.max(np.abs(g - r)) / max(1e-30, np.max(np.abs(r)))
+        assert err <= REL_TOL, (w.name, name, err)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 17), (1, 1, 128), (2, 1, 129),
+                                   (1, 2, 300), (1, 1, 513), (2, 2, 1000)])
+def test_small_shapes_full(attn_lib, dtype, causal, B, H, N):
+    w = wl.Workload(f"bwd_{B}x{H}x{N}", "bwd", B, H, N, 128, dtype, causal, seed=7 + N)
+    inp = wl.make_inputs(w)
+    grads = _gpu_grads(attn_lib, inp, w)
+    refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), causal,
+                                     w.scale)
+    _check(w, grads, refs)
+
+
+def test_bf16_backward_workload(attn_lib):
+    """[2,16,8192,128] bf16 causal; the oracle recomputes two whole heads."""
+    w = wl.BWD_BF16_D128
+    inp = wl.make_inputs(w)
+    grads = _gpu_grads(attn_lib, inp, w)
+    heads = [(0, 0), (1, 15)]
+    refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), True,
+                                     w.scale, heads=heads)
+    _check(w, grads, refs, heads)
+
+
+def test_noncausal_medium(attn_lib):
+    w = wl.Workload("bwd_nc", "bwd", 1, 4, 2048, 128, "bf16", False, seed=3)
+    inp = wl.make_inputs(w)
+    grads = _gpu_grads(attn_lib, inp, w)
+    heads = sample_heads(1, 4, 2, seed=1)
+    refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), False,
+                                     w.scale, heads=heads)
+    _check(w, grads, refs, heads)
+
+
+def test_q_zero_closed_forms(attn_lib):
+    """Q = 0, causal: dK = 0 exactly and dV_j = sum_{i>=j} dO_i / (i+1)."""
+    w = wl.Workload("bwd_q0", "bwd", 1, 2, 1500, 128, "bf16", True, seed=11)
+    inp = wl.make_inputs(w)
+    inp["q"] = torch.zeros_like(inp["q"])
+    dq, dk, dv = _gpu_grads(attn_lib, inp, w)
+    assert torch.count_nonzero(dk) == 0
+    do = to64(inp["do"][0, 1])
+    want = np.cumsum((do / np.arange(1, w.N + 1)[:, None])[::-1], axis=0)[::-1]
+    err = np.max(np.abs(to64(dv[0, 1]) - want)) / np.max(np.abs(want))
+    assert err <= REL_TOL
+
+
+def test_bwd_argument_errors(attn_lib):
+    L = attn_lib.lib()
+    x = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 64), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    p, pl, pw = (ctypes.c_void_p(t.data_ptr()) for t in (x, lse, ws))
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    need = attn_lib.bwd_workspace_bytes(1, 1, 64, 128)
+    args = lambda d, wsz: (p, p, p, p, p, pl, p, p, p, pw, wsz, 1, 1, 64, d, 1, 0.1, 1, s)  # noqa
+    assert L.attn_bwd(*args(64, need)) == 2            # d = 64 unsupported
+    assert L.attn_bwd(*args(128, need - 1)) == 1       # workspace too small
+    assert L.attn_bwd(*args(128, need)) == 0
+    assert attn_lib.poll_status()[0] == 0
