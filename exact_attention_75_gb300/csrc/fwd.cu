@@ -22,13 +22,22 @@
 // recast for an MMA warp that issues for both tiles).
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
-//   [  0,128) S_0 (fp32); P_0 (16-bit, packed in pairs) overwrites [0,64)
+//   [  0,128) S_0 (fp32); P_0 overwrites [0,64) (16-bit pairs) or [0,32)
+//             (E4M3 quads)
 //   [128,256) S_1 / P_1
 //   [256,256+D) O_0 (fp32)     [256+D,256+2D) O_1
+//
+// Precisions: fp16 and bf16 (kind::f16 MMAs; V is the MN-major B operand of
+// P V), and E4M3 ("8.3 FlashAttention-3", section 5: kind::f8f6f4 MMAs with
+// fp32 accumulation).  In the E4M3 path S_ij = q8_i.k8_j sq(i/64) sk(j/64),
+// V arrives transposed (a K-major B operand), and P is stored as E4M3 after
+// multiplying it by sv(j/64)/max(sv): the reference max keeps P <= 2^8, so
+// the product fits E4M3, and O = max(sv) * sum(P~ V8) / l.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "fp8.cuh"
 #include "fwd.cuh"
 #include "sm103_ptx.cuh"
 #include "tiles.cuh"
@@ -41,11 +50,12 @@ constexpr int kThreads = 320;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+constexpr int kPrecF16 = 0, kPrecBF16 = 1, kPrecE4M3 = 2;
 
-template <int D>
+template <int D, bool FP8>
 struct FwdLayout {
-  static constexpr int kTileBytes = 128 * D * 2;       // 128 rows x D 16-bit values
-  static constexpr int kSlots = (D == 128) ? 4 : 8;    // K/V ring depth (tiles)
+  static constexpr int kTileBytes = 128 * D * (FP8 ? 1 : 2);  // 128 rows x D values
+  static constexpr int kSlots = (FP8 || D == 64) ? 8 : 4;     // K/V ring depth (tiles)
   static constexpr int kQOff = 0;
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kSlots * kTileBytes;
@@ -88,11 +98,19 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   return w;
 }
 
-template <int D, bool CAUSAL, bool BF16>
+// E4M3 K-major operand: one 128-byte swizzle atom column per 128 rows; step
+// k32 selects 32 values (bytes) of the reduction dimension.
+__device__ __forceinline__ uint64_t kmajor_desc8(uint32_t tile_addr, int k32) {
+  return sdesc_sw128(tile_addr + (uint32_t)k32 * 32u, 16, 1024);
+}
+
+template <int D, bool CAUSAL, int PREC>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using L = FwdLayout<D>;
+  constexpr bool FP8 = PREC == kPrecE4M3;
+  constexpr bool BF16 = PREC == kPrecBF16;
+  using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -151,10 +169,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
           const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
+          if constexpr (FP8) {
+            tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, (2 * w.qp + t) * 128, w.bh);
+          } else {
 #pragma unroll
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(dst + h * 16384, &tmQ, bar(L::kQFull + t), h * 64,
-                        (2 * w.qp + t) * 128, w.bh);
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(dst + h * 16384, &tmQ, bar(L::kQFull + t), h * 64,
+                          (2 * w.qp + t) * 128, w.bh);
+          }
           ++q_it[t];
         }
         const int nbmax = max(w.nb[0], w.nb[1]);
@@ -166,10 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(bar(L::kKvFull + slot), L::kTileBytes);
             const uint32_t dst = sbase + L::kKvOff + slot * L::kTileBytes;
+            if constexpr (FP8) {
+              // K: [128 keys][128 d] bytes; V^T: [128 d][128 keys] bytes.
+              if (which == 0)
+                tma_load_3d(dst, &tmK, bar(L::kKvFull + slot), 0, j * 128, w.bh);
+              else
+                tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), j * 128, 0, w.bh);
+            } else {
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h)
-              tma_load_3d(dst + h * 16384, which ? &tmV : &tmK, bar(L::kKvFull + slot), h * 64,
-                          j * 128, w.bh);
+              for (int h = 0; h < D / 64; ++h)
+                tma_load_3d(dst + h * 16384, which ? &tmV : &tmK, bar(L::kKvFull + slot),
+                            h * 64, j * 128, w.bh);
+            }
             ++kv_it;
           }
         }
@@ -189,11 +219,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------- tcgen05 issuer ---
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t kIdO = idesc_f16(128, D, BF16, false, true);
+      constexpr uint32_t kIdS =
+          FP8 ? idesc_e4m3(128, 128, false, false) : idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t kIdO =
+          FP8 ? idesc_e4m3(128, D, false, false) : idesc_f16(128, D, BF16, false, true);
       uint32_t kv_it = 0, q_it[2] = {0, 0}, p_it[2] = {0, 0};
       bool ok = true;
       const uint32_t qaddr[2] = {sbase + L::kQOff, sbase + L::kQOff + L::kTileBytes};
+      // S_t = Q_t K^T into tensor-memory columns [128t, 128t+128).
+      auto issue_s = [&](int t, uint32_t kaddr) {
+        if constexpr (FP8) {
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_f8_ss(tbase + 128 * t, kmajor_desc8(qaddr[t], kk), kmajor_desc8(kaddr, kk), kIdS,
+                      kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16_ss(tbase + 128 * t, kmajor_desc16(qaddr[t], kk), kmajor_desc16(kaddr, kk),
+                       kIdS, kk > 0);
+        }
+      };
       for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, G);
         if (u >= p.num_units) break;
@@ -213,11 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int t = 0; t < 2; ++t) {
           if (w.nb[t] == 0) continue;
-          const uint32_t kaddr = sbase + L::kKvOff + kslot * L::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_f16_ss(tbase + 128 * t, kmajor_desc16(qaddr[t], kk), kmajor_desc16(kaddr, kk),
-                       kIdS, kk > 0);
+          issue_s(t, sbase + L::kKvOff + kslot * L::kTileBytes);
           mma_commit(bar(L::kSFull + t));
           if (w.nb[t] == 1) mma_commit(bar(L::kQEmpty + t));
         }
@@ -242,18 +284,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++p_it[t];
             tc_fence_after();
-            // O_t += P_t V_j  (A = P from tensor memory, 16 keys per MMA)
+            // O_t += P_t V_j  (A = P from tensor memory)
             const uint32_t ocol = tbase + 256 + D * t;
+            if constexpr (FP8) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ts(ocol, tbase + 128 * t + kk * 8, mnmajor_desc16(vaddr, kk), kIdO,
-                         (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)  // 32 keys per MMA
+                mma_f8_ts(ocol, tbase + 128 * t + kk * 8, kmajor_desc8(vaddr, kk), kIdO,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA
+                mma_f16_ts(ocol, tbase + 128 * t + kk * 8, mnmajor_desc16(vaddr, kk), kIdO,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+            }
             if (j == w.nb[t] - 1) mma_commit(bar(L::kOFull + t));
             if (j + 1 < w.nb[t]) {
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                mma_f16_ss(tbase + 128 * t, kmajor_desc16(qaddr[t], kk),
-                           kmajor_desc16(kaddr, kk), kIdS, kk > 0);
+              issue_s(t, kaddr);
               mma_commit(bar(L::kSFull + t));
               if (j + 1 == w.nb[t] - 1) mma_commit(bar(L::kQEmpty + t));
             }
@@ -289,8 +335,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nb == 0) continue;
       const int tile = 2 * w.qp + t;
       const int row = tile * 128 + r;
-      float m = -INFINITY;  // running max of scale*log2(e)*s (reference value)
+      float m = -INFINITY;  // running max of the log2-scaled scores (reference value)
       float l = 0.f;        // running sum of exp2(x - m)
+      // E4M3 path: this row's Q block scale and the head's largest V scale
+      // (warp-shuffle max over the V block scales).
+      float fq = 0.f, sv_max = 1.f;
+      const float* ksc = nullptr;
+      const float* vsc = nullptr;
+      if constexpr (FP8) {
+        const size_t sb = (size_t)w.bh * p.n_sblocks;
+        ksc = p.k_scale + sb;
+        vsc = p.v_scale + sb;
+        fq = p.q_scale[sb + min(row, p.N - 1) / 64] * sl2;
+        float mv = 0.f;
+        for (int b = lane; b < p.n_sblocks; b += 32) mv = fmaxf(mv, vsc[b]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+        sv_max = mv > 0.f ? mv : 1.f;
+      }
       for (int j = 0; j < nb; ++j) {
         ok = mbar_wait(bar(L::kSFull + t), s_it & 1, wd, 11);
         ok = __all_sync(0xffffffffu, ok);
@@ -304,10 +367,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
         float s[128];
+        float g0 = 1.f, g1 = 1.f;
+        if constexpr (FP8) {
+          // keys [0,64) and [64,128) of block j have their own K and V scales
+          const int b0 = 2 * j, b1 = min(2 * j + 1, p.n_sblocks - 1);
+          const float f0 = fq * ksc[b0];
+          const float f1 = fq * ksc[b1];
+          g0 = vsc[b0] / sv_max;
+          g1 = vsc[b1] / sv_max;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+            for (int i = 0; i < 32; ++i)
+              s[c * 32 + i] = __uint_as_float(sr[c][i]) * (c < 2 ? f0 : f1);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+        }
         const bool diag = CAUSAL && (j == tile);
         const bool tail = (j == p.n_kblocks - 1) && (p.N & 127);
         if (diag || tail) {
@@ -319,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mx = s[0];
 #pragma unroll
         for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        const float m_blk = mx * sl2;
+        const float m_blk = FP8 ? mx : mx * sl2;
         if (j == 0) {
           m = m_blk;
         } else {
@@ -349,17 +427,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float mref = (m == -INFINITY) ? 0.f : m;
         float rowsum = 0.f;
+        if constexpr (FP8) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
-            const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
-            rowsum += p0 + p1;
-            pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            for (int i = 0; i < 16; ++i) {
+              float pv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = c * 64 + 4 * i + e;
+                pv[e] = ex2_approx(s[col] - mref);
+                rowsum += pv[e];
+                pv[e] *= (c == 0 ? g0 : g1);
+              }
+              pk[i] = (uint32_t)pack_e4m3x2(pv[0], pv[1]) |
+                      ((uint32_t)pack_e4m3x2(pv[2], pv[3]) << 16);
+            }
+            tmem_st16(s_addr + c * 16, pk);
           }
-          tmem_st16(s_addr + c * 16, pk);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
+              const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
+              rowsum += p0 + p1;
+              pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            }
+            tmem_st16(s_addr + c * 16, pk);
+          }
         }
         l += rowsum;
         tmem_wait_st();
@@ -373,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++o_it;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = (FP8 ? sv_max : 1.0f) / l;
       const size_t grow = (size_t)w.bh * p.N + row;
       uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
 #pragma unroll
@@ -385,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) {
           const float a = __uint_as_float(raw[2 * i]) * inv_l;
           const float b = __uint_as_float(raw[2 * i + 1]) * inv_l;
-          pk[i] = BF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+          pk[i] = (BF16 || FP8) ? pack_bf16x2(a, b) : pack_f16x2(a, b);
         }
         if (row < p.N) {
 #pragma unroll
@@ -406,10 +505,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
-cudaError_t launch_one(const FwdLaunch& a) {
-  using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL, BF16>;
+template <int D, bool CAUSAL, int PREC>
+cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const FwdParams& params, int num_ctas, cudaStream_t stream) {
+  using L = FwdLayout<D, PREC == kPrecE4M3>;
+  auto kern = fwd_kernel<D, CAUSAL, PREC>;
   static bool configured = false;  // attribute set once per instantiation
   if (!configured) {
     cudaError_t e =
@@ -417,20 +517,39 @@ cudaError_t launch_one(const FwdLaunch& a) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int grid = a.params.num_units < a.num_ctas ? a.params.num_units : a.num_ctas;
-  kern<<<grid, kThreads, L::kDynSmem, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.params);
+  const int grid = params.num_units < num_ctas ? params.num_units : num_ctas;
+  kern<<<grid, kThreads, L::kDynSmem, stream>>>(tmQ, tmK, tmV, params);
   return cudaGetLastError();
+}
+
+template <int D, int PREC>
+cudaError_t launch_dc(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                      const FwdParams& p, int n, cudaStream_t s, bool causal) {
+  return causal ? launch_one<D, true, PREC>(q, k, v, p, n, s)
+                : launch_one<D, false, PREC>(q, k, v, p, n, s);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, int d, bool causal, bool bf16) {
-  if (d == 128) {
-    if (causal) return bf16 ? launch_one<128, true, true>(a) : launch_one<128, true, false>(a);
-    return bf16 ? launch_one<128, false, true>(a) : launch_one<128, false, false>(a);
-  }
-  if (causal) return bf16 ? launch_one<64, true, true>(a) : launch_one<64, true, false>(a);
-  return bf16 ? launch_one<64, false, true>(a) : launch_one<64, false, false>(a);
+  const auto& q = a.tmQ;
+  const auto& k = a.tmK;
+  const auto& v = a.tmV;
+  if (d == 128)
+    return bf16 ? launch_dc<128, kPrecBF16>(q, k, v, a.params, a.num_ctas, a.stream, causal)
+                : launch_dc<128, kPrecF16>(q, k, v, a.params, a.num_ctas, a.stream, causal);
+  return bf16 ? launch_dc<64, kPrecBF16>(q, k, v, a.params, a.num_ctas, a.stream, causal)
+              : launch_dc<64, kPrecF16>(q, k, v, a.params, a.num_ctas, a.stream, causal);
+}
+
+cudaError_t launch_fwd_fp8(const Fp8FwdLaunch& a) {
+  FwdParams p = a.base.params;
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.n_sblocks = (p.N + 63) / 64;
+  return launch_dc<128, kPrecE4M3>(a.tmQ, a.tmK, a.tmVt, p, a.base.num_ctas, a.base.stream,
+                                   a.causal);
 }
 
 }  // namespace attn

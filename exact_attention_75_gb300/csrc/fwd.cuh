@@ -18,6 +18,11 @@ struct FwdParams {
   int num_units;        // BH * n_pairs
   float scale_log2;     // scale * log2(e)
   unsigned long long wait_limit_ns;
+  // E4M3 path only: per-(head, 64-row block) fp32 scales of Q, K and V.
+  const float* q_scale = nullptr;
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
+  int n_sblocks = 0;    // ceil(N / 64)
 };
 
 struct FwdLaunch {

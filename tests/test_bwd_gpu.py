@@ -36,7 +36,14 @@ def _check(w, grads, refs, heads=None):
         if heads is not None:
             g = np.stack([g[b, h] for b, h in heads])
             r = np.stack([r[b, h] for b, h in heads])
-        err = np.max(np.abs(g - r)) / max(1e-30, np.max(np.abs(r)))
+        ref_max = np.max(np.abs(r))
+        if ref_max == 0.0:
+            # The gradient is exactly zero in exact arithmetic (e.g. N = 1:
+            # the softmax over a single key has zero Jacobian); a relative
+            # error is undefined, so bound the rounding noise absolutely.
+            assert np.max(np.abs(g)) <= 1e-3, (w.name, name)
+            continue
+        err = np.max(np.abs(g - r)) / ref_max
         assert err <= REL_TOL, (w.name, name, err)
 
 
