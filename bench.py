@@ -118,6 +118,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# ------------------------------------------------------------ ranks --------
+
+def max_over_ranks(values):
+    """Element-wise max of per-rank timings (a host-side timing reduction,
+    not part of the data path).  NCCL needs the tensor on the GPU, gloo on
+    the CPU."""
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
+    """Weak scaling: rank r owns global heads [r*B*H, (r+1)*B*H) of a job of
+    world*B*H independent heads; its slice is drawn with seed r."""
+    return w.with_(seed=w.seed + rank)
+
+
 # ------------------------------------------------------------ GPU arm -------
 
 class Step:
@@ -220,7 +238,7 @@ def run_gpu(args, rank, world, local_rank):
             if "UNSUPPORTED" not in str(e):
                 raise
     del trial
-    st = Step(attn, w, dev, comps)
+    st = Step(attn, rank_workload(w, rank), dev, comps)
     flops = component_flops(w)
     nbytes = component_bytes(w)
     stream = torch.cuda.current_stream()
@@ -287,9 +305,7 @@ def run_gpu(args, rank, world, local_rank):
     step_flops = sum(flops[c] for c in comps)
     ms_step = ms_total / args.steps
     if world > 1:
-        t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
+        ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
     return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks,
                 flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
                 launches=sum(LAUNCHES[c] for c in comps) * args.steps)

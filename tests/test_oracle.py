@@ -342,3 +342,24 @@ def test_golden_fa3_table_decoding():
         assert raw.startswith(row["seqlen"])
         assert raw == f'{row["seqlen"]}{row["fa2"]}{row["fa3"]}{row["speedup"]:.2f}x'
         assert abs(row["fa3"] / row["fa2"] - row["speedup"]) < 0.006
+
+
+def test_fp8_recipe_error_floor():
+    """The prescribed FP8 recipe (per-64-row E4M3 scales, Hadamard on Q and K)
+    evaluated in fp64 on the dequantized inputs, with no kernel involved:
+    on N(0,1) inputs its RMSE(O) is far below 3e-2; with 0.1% of entries x20
+    it is already above 3e-2.  This is why the FP8 outlier workload is held to
+    the quantization-aware oracle (see tests/test_fp8_gpu.py)."""
+    res = {}
+    for outl in (False, True):
+        w = Workload("t", "fwd_fp8", 1, 1, 1024, 128, "bf16", True, outliers=outl,
+                     hadamard=True, seed=3)
+        inp = make_inputs(w)
+        q, k, v = (np.asarray(inp[n].to(torch.float64)) for n in ("q", "k", "v"))
+        s = inp["signs"].numpy()
+        dq = lambda x, sg=None: oracle.dequantize_blocks(  # noqa: E731
+            *[oracle.quantize_blocks(x, 64, sg)[y] for y in ("codes", "scales")], 64)
+        O_ref, _ = oracle.attention(q, k, v, True, w.scale)
+        O_q, _ = oracle.attention(dq(q, s), dq(k, s), dq(v), True, w.scale)
+        res[outl] = oracle.rmse(O_q, O_ref)
+    assert res[False] < 0.01 and res[True] > 0.03, res
