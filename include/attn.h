@@ -99,6 +99,33 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      int causal, float scale, attn_dtype dtype, void* stream);
 
 /*
+ * Backward pass that allocates nothing (no counterpart on the pages: it is a
+ * library convenience, not part of the method).
+ *
+ * For callers that cannot hand attn_bwd a workspace: plugins whose host
+ * framework owns all device memory and exposes no raw allocations, serving
+ * loops that must not call cudaMalloc (which can synchronise the device) on
+ * the request path, or programs with a fixed memory plan.  It computes the
+ * same dQ, dK, dV as attn_bwd, with the same arguments minus the workspace;
+ * the scratch (delta + fp32 dQ accumulator) lives in a fixed device array
+ * inside the library.
+ *   Limit: B*H*N <= 65536 query rows and d = 128; larger problems return
+ *   ATTN_ERR_INVALID_ARG, other head dims ATTN_ERR_UNSUPPORTED.
+ *   Memory: the array (about 33.8 MB) is part of the library image and is
+ *   held on every GPU that loads the library until the process exits.
+ *   Sharing: all calls use the same array.  The call zeroes what must start
+ *   at zero, but calls that overlap on the GPU (different streams, or
+ *   different host threads, without ordering between them) race on it.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that
+ *   first call before any stream capture.
+ */
+attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             int B, int H, int N, int d, int causal, float scale,
+                             attn_dtype dtype, void* stream);
+
+/*
  * FP8 E4M3 block quantization of one bf16 tensor, optionally after the
  * randomized Hadamard rotation x <- x H_d diag(signs) / sqrt(d).
  *   x_bf16  : [B,H,N,d] bf16, read only.

@@ -1,0 +1,72 @@
+"""attn_bwd_noalloc: the backward pass for callers that cannot allocate.
+
+Callers such as plugins whose host framework owns every device allocation,
+or serving loops that may not call cudaMalloc on the request path, use this
+entry point instead of attn_bwd: it keeps its scratch in a fixed device array
+inside the library, so the call allocates nothing.  This file checks it
+through the C ABI against attn_bwd (same inputs, the backward tolerance
+5e-2 * max |reference|) on two calls in a row, and that oversized problems are
+rejected.  It is named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from helpers import to64
+
+pytestmark = pytest.mark.gpu
+REL_TOL = 5e-2
+MAX_ROWS = 65536  # B * H * N limit of the fixed scratch array
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _noalloc_fn(attn):
+    L = attn.lib()
+    fn = L.attn_bwd_noalloc
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp]
+    fn.restype = i
+    return fn
+
+
+def _call(fn, q, k, v, o, do, lse, dq, dk, dv, w, stream):
+    return fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+              _ptr(dv), w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), 1, stream)
+
+
+def test_noalloc_backward_matches_attn_bwd_twice(attn_lib):
+    fn = _noalloc_fn(attn_lib)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # two different problems in a row through the shared scratch array
+    for w in (wl.Workload("na1", "bwd", 1, 4, 1000, 128, "bf16", True, seed=31),
+              wl.Workload("na2", "bwd", 2, 3, 4096, 128, "bf16", False, seed=32)):
+        inp = wl.make_inputs(w)
+        q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+        o, lse = attn_lib.fwd(q, k, v, causal=w.causal, scale=w.scale)
+        ref = attn_lib.bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale)
+        got = [torch.full_like(q, float("nan")) for _ in range(3)]
+        assert _call(fn, q, k, v, o, do, lse, *got, w, stream) == 0
+        st, detail = attn_lib.poll_status()
+        assert st == 0, hex(detail)
+        for g, r in zip(got, ref):
+            g, r = to64(g), to64(r)
+            assert np.isfinite(g).all()
+            assert np.max(np.abs(g - r)) <= REL_TOL * np.max(np.abs(r))
+
+
+def test_noalloc_rejects_oversized_problems(attn_lib):
+    fn = _noalloc_fn(attn_lib)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    x = torch.zeros((1, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 16), dtype=torch.float32, device="cuda")
+    big = wl.Workload("big", "bwd", 1, 1, MAX_ROWS + 1, 128, "bf16", True)
+    assert _call(fn, x, x, x, x, x, lse, x, x, x, big, stream) == 1  # ATTN_ERR_INVALID_ARG
+    d64 = wl.Workload("d64", "bwd", 1, 1, 16, 64, "bf16", True)
+    assert _call(fn, x, x, x, x, x, lse, x, x, x, d64, stream) == 2  # ATTN_ERR_UNSUPPORTED
+    assert attn_lib.poll_status()[0] == 0
