@@ -234,6 +234,9 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   p.dv = dv;
   p.delta = static_cast<float*>(workspace);
   p.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dbytes);
+  if (!encode_3d(&a.tmDQacc, p.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, 128, 32,
+                 CU_TENSOR_MAP_SWIZZLE_NONE))
+    return ATTN_ERR_CUDA;
   p.status = di->status;
   p.BH = (int)BH;
   p.N = N;

@@ -13,7 +13,7 @@
 //                       dP^T = V dO_i^T, dS^T = P^T o (dP^T - D_i), and
 //                       accumulates dV += P^T dO_i, dK += dS^T Q_i in tensor
 //                       memory; dQ_i^T = K^T dS^T is drained into the fp32
-//                       accumulator with atomic adds;
+//                       accumulator with TMA bulk reduce-adds;
 //   3. bwd_post_kernel  dQ = scale * dQ_acc, rounded to 16 bit.
 //
 // Main-kernel CTA organisation (320 threads):
@@ -94,7 +94,7 @@ template <bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdLayout;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -317,7 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = st_it & 1;
         ok = mbar_wait(bar(L::kSFull + h), s_it & 1, wd, 31);
         ok = ok && mbar_wait(bar(L::kQFull + stage), (st_it >> 1) & 1, wd, 32);
-        ok = __all_sync(0xffffffffu, ok);
+        // Exit decisions are uniform over the warpgroup: its four warps meet
+        // at named barriers further down.
+        ok = named_bar_and(1 + h, 128, ok);
         if (!ok) break;
         ++s_it;
         tc_fence_after();
@@ -370,29 +372,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(L::kPFull + h));
         // dQ^T_h: TMEM lane = head-dim index r, column = query of this half.
         ok = mbar_wait(bar(L::kDqFull + h), (s_it - 1) & 1, wd, 33);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = named_bar_and(1 + h, 128, ok);
         if (!ok) break;
         tc_fence_after();
-        const int q0 = i * 128 + 64 * h;
-        float* acc = p.dq_acc + ((size_t)w.bh * p.N + q0) * 128 + r;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t qr[32];
-          tmem_ld32_sync(s_addr + 32 * c, qr);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = 32 * c + e;
-            if (q0 + col < p.N) atomicAdd(acc + (size_t)col * 128, __uint_as_float(qr[e]));
-          }
-        }
+        uint32_t qa[32], qb[32];
+        tmem_ld32(s_addr, qa);
+        tmem_ld32(s_addr + 32, qb);
+        tmem_wait_ld();
+        reg_fence32(qa);
+        reg_fence32(qb);
+        // The columns are free again: the next S^T_h may be issued now.
         tc_fence_before();
         mbar_arrive(bar(L::kDqFree + h));
+        // Reduce into the fp32 accumulator with TMA bulk reduce-add, staging
+        // 32 queries x 128 values (16 KB) at a time in this half's dS^T
+        // buffer, which the completed dQ^T MMA no longer reads.  Rows at or
+        // beyond N fall outside the tensor map and are dropped by the TMA.
+        float* qstage = reinterpret_cast<float*>(smem + L::kDS + 16384 * h);
+        const bool leader = (threadIdx.x & 127) == 0;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c == 1) {
+            if (leader) bulk_wait_group_read0();
+            named_bar_sync(1 + h, 128);
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) qstage[e * 128 + r] = __uint_as_float(c == 0 ? qa[e] : qb[e]);
+          fence_proxy_async_smem();
+          named_bar_sync(1 + h, 128);
+          if (leader) {
+            tma_reduce_add_3d(&tmDQ, smem_u32(qstage), 0, i * 128 + 64 * h + 32 * c, w.bh);
+            bulk_commit_group();
+          }
+        }
+        // The buffer is rewritten by the next step's dS^T: wait for the reads.
+        if (leader) bulk_wait_group_read0();
+        named_bar_sync(1 + h, 128);
         ++st_it;
       }
       if (!ok) break;
       // ---------------------------------------------------- dK / dV epilogue ---
       ok = mbar_wait(bar(L::kDkvFull), unit_it & 1, wd, 34);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = named_bar_and(1 + h, 128, ok);
       if (!ok) break;
       ++unit_it;
       tc_fence_after();
@@ -423,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (warp < 8 && (threadIdx.x & 127) == 0) bulk_wait_group0();  // dQ reductions landed
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -504,7 +526,8 @@ cudaError_t launch_main(const BwdLaunch& a) {
   }
   const int units = a.params.BH * a.params.n_kblocks;
   const int grid = units < a.num_sms ? units : a.num_sms;
-  kern<<<grid, kThreads, BwdLayout::kBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, a.params);
+  kern<<<grid, kThreads, BwdLayout::kBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, a.tmDQacc,
+                                                        a.params);
   return cudaGetLastError();
 }
 

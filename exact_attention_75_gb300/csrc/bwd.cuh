@@ -30,6 +30,7 @@ struct BwdParams {
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;
+  CUtensorMap tmDQacc;   // fp32 [B*H, N, 128], box 128 x 32, no swizzle (reduce-add)
   BwdParams params;
   int num_sms;
   cudaStream_t stream;
