@@ -317,6 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = st_it & 1;
         ok = mbar_wait(bar(L::kSFull + h), s_it & 1, wd, 31);
         ok = ok && mbar_wait(bar(L::kQFull + stage), (st_it >> 1) & 1, wd, 32);
+        // The dS^T buffer doubles as the dQ staging area of the previous
+        // step: its TMA reads must be done before dS^T is written again.
+        if ((threadIdx.x & 127) == 0) bulk_wait_group_read0();
         // Exit decisions are uniform over the warpgroup: its four warps meet
         // at named barriers further down.
         ok = named_bar_and(1 + h, 128, ok);
@@ -405,9 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_group();
           }
         }
-        // The buffer is rewritten by the next step's dS^T: wait for the reads.
-        if (leader) bulk_wait_group_read0();
-        named_bar_sync(1 + h, 128);
         ++st_it;
       }
       if (!ok) break;

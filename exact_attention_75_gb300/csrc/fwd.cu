@@ -394,9 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
-        float mx = s[0];
+        // Row max as 8 independent chains (a single 128-long fmaxf chain is
+        // latency-bound).
+        float mx8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < 8; ++c) mx8[c] = s[c];
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+#pragma unroll
+        for (int c = 4; c > 0; c >>= 1)
+#pragma unroll
+          for (int e = 0; e < c; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + c]);
+        const float mx = mx8[0];
         const float m_blk = FP8 ? mx : mx * sl2;
         if (j == 0) {
           m = m_blk;
@@ -426,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float mref = (m == -INFINITY) ? 0.f : m;
-        float rowsum = 0.f;
+        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
         if constexpr (FP8) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -438,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 4; ++e) {
                 const int col = c * 64 + 4 * i + e;
                 pv[e] = ex2_approx(s[col] - mref);
-                rowsum += pv[e];
+                rs[(4 * i + e) & 7] += pv[e];
                 pv[e] *= (c == 0 ? g0 : g1);
               }
               pk[i] = (uint32_t)pack_e4m3x2(pv[0], pv[1]) |
@@ -454,13 +463,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i) {
               const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
               const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
-              rowsum += p0 + p1;
+              rs[(2 * i) & 7] += p0;
+              rs[(2 * i + 1) & 7] += p1;
               pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
             }
             tmem_st16(s_addr + c * 16, pk);
           }
         }
-        l += rowsum;
+#pragma unroll
+        for (int c = 4; c > 0; c >>= 1)
+#pragma unroll
+          for (int e = 0; e < c; ++e) rs[e] += rs[e + c];
+        l += rs[0];
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::kPFull + t));
