@@ -220,7 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_it = 0, st_it = 0, unit_it = 0;
       uint32_t dq_it[2] = {0, 0}, p_it[2] = {0, 0};
       bool ok = true;
-      const uint32_t kaddr = sbase + L::kK, vaddr = sbase + L::kV;
+      // Base descriptors: K and V as K-major A operands of S^T / dP^T, K as
+      // the MN-major A operand of dQ^T, the dS^T halves as MN-major B.
+      const uint64_t kd_k = kmajor_base(sbase + L::kK), vd_k = kmajor_base(sbase + L::kV);
+      const uint64_t kd_mn = mnmajor_base(sbase + L::kK);
+      const uint64_t dsd[2] = {mnmajor_base(sbase + L::kDS), mnmajor_base(sbase + L::kDS + 16384)};
       for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, G);
         if (u >= num_units) break;
@@ -242,14 +246,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
+            const uint64_t qd = kmajor_base(qaddr + 8192u * h);
+            const uint64_t dod = kmajor_base(doaddr + 8192u * h);
+            const uint32_t cs = tbase + col_s(h), cdp = tbase + col_dp(h);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(tbase + col_s(h), kmajor_desc16(kaddr, kk),
-                         kmajor_desc16(qaddr + 8192u * h, kk), kIdS, kk > 0);
+              mma_f16_ss(cs, desc_plus(kd_k, kmajor16_off(kk)), desc_plus(qd, kmajor16_off(kk)),
+                         kIdS, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(tbase + col_dp(h), kmajor_desc16(vaddr, kk),
-                         kmajor_desc16(doaddr + 8192u * h, kk), kIdS, kk > 0);
+              mma_f16_ss(cdp, desc_plus(vd_k, kmajor16_off(kk)), desc_plus(dod, kmajor16_off(kk)),
+                         kIdS, kk > 0);
             mma_commit(bar(L::kSFull + h));
           }
           if (!ok) break;
@@ -263,20 +270,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++p_it[h];
             tc_fence_after();
+            const uint64_t dod_mn = mnmajor_base(doaddr + 8192u * h);
+            const uint64_t qd_mn = mnmajor_base(qaddr + 8192u * h);
+            const uint32_t acc0 = (s > 0 || h > 0) ? 1u : 0u;
+            const uint32_t cs = tbase + col_s(h), cdp = tbase + col_dp(h);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ts(tbase + kColDV, tbase + col_s(h) + 8 * kk,
-                         mnmajor_desc16(doaddr + 8192u * h, kk), kIdKV,
-                         (s > 0 || h > 0 || kk > 0) ? 1u : 0u);
+              mma_f16_ts(tbase + kColDV, cs + 8 * kk, desc_plus(dod_mn, mnmajor16_off(kk)), kIdKV,
+                         kk > 0 ? 1u : acc0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ts(tbase + kColDK, tbase + col_dp(h) + 8 * kk,
-                         mnmajor_desc16(qaddr + 8192u * h, kk), kIdKV,
-                         (s > 0 || h > 0 || kk > 0) ? 1u : 0u);
-            const uint32_t dsaddr = sbase + L::kDS + 16384u * h;
+              mma_f16_ts(tbase + kColDK, cdp + 8 * kk, desc_plus(qd_mn, mnmajor16_off(kk)), kIdKV,
+                         kk > 0 ? 1u : acc0);
+            const uint64_t dsb = h ? dsd[1] : dsd[0];
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(tbase + col_s(h), mnmajor_desc16(kaddr, kk), mnmajor_desc16(dsaddr, kk),
+              mma_f16_ss(cs, desc_plus(kd_mn, mnmajor16_off(kk)), desc_plus(dsb, mnmajor16_off(kk)),
                          kIdQ, kk > 0);
             mma_commit(bar(L::kDqFull + h));
             ++dq_it[h];

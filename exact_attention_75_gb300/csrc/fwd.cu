@@ -98,12 +98,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   return w;
 }
 
-// E4M3 K-major operand: one 128-byte swizzle atom column per 128 rows; step
-// k32 selects 32 values (bytes) of the reduction dimension.
-__device__ __forceinline__ uint64_t kmajor_desc8(uint32_t tile_addr, int k32) {
-  return sdesc_sw128(tile_addr + (uint32_t)k32 * 32u, 16, 1024);
-}
-
 template <int D, bool CAUSAL, int PREC>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -225,18 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           FP8 ? idesc_e4m3(128, D, false, false) : idesc_f16(128, D, BF16, false, true);
       uint32_t kv_it = 0, q_it[2] = {0, 0}, p_it[2] = {0, 0};
       bool ok = true;
-      const uint32_t qaddr[2] = {sbase + L::kQOff, sbase + L::kQOff + L::kTileBytes};
+      // Base descriptors of the two Q tiles (K-major); K-steps add constants.
+      const uint64_t qdesc[2] = {kmajor_base(sbase + L::kQOff),
+                                 kmajor_base(sbase + L::kQOff + L::kTileBytes)};
       // S_t = Q_t K^T into tensor-memory columns [128t, 128t+128).
       auto issue_s = [&](int t, uint32_t kaddr) {
+        const uint64_t kd = kmajor_base(kaddr);
+        const uint64_t qd = t ? qdesc[1] : qdesc[0];
+        const uint32_t dcol = tbase + 128 * t;
         if constexpr (FP8) {
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)
-            mma_f8_ss(tbase + 128 * t, kmajor_desc8(qaddr[t], kk), kmajor_desc8(kaddr, kk), kIdS,
-                      kk > 0);
+            mma_f8_ss(dcol, desc_plus(qd, 32 * kk), desc_plus(kd, 32 * kk), kIdS, kk > 0);
         } else {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_f16_ss(tbase + 128 * t, kmajor_desc16(qaddr[t], kk), kmajor_desc16(kaddr, kk),
+            mma_f16_ss(dcol, desc_plus(qd, kmajor16_off(kk)), desc_plus(kd, kmajor16_off(kk)),
                        kIdS, kk > 0);
         }
       };
@@ -286,16 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // O_t += P_t V_j  (A = P from tensor memory)
             const uint32_t ocol = tbase + 256 + D * t;
+            const uint32_t pcol = tbase + 128 * t;
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
             if constexpr (FP8) {
+              const uint64_t vd = kmajor_base(vaddr);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)  // 32 keys per MMA
-                mma_f8_ts(ocol, tbase + 128 * t + kk * 8, kmajor_desc8(vaddr, kk), kIdO,
-                          (j > 0 || kk > 0) ? 1u : 0u);
+                mma_f8_ts(ocol, pcol + kk * 8, desc_plus(vd, 32 * kk), kIdO, kk > 0 ? 1u : acc0);
             } else {
+              const uint64_t vd = mnmajor_base(vaddr);
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA
-                mma_f16_ts(ocol, tbase + 128 * t + kk * 8, mnmajor_desc16(vaddr, kk), kIdO,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_f16_ts(ocol, pcol + kk * 8, desc_plus(vd, mnmajor16_off(kk)), kIdO,
+                           kk > 0 ? 1u : acc0);
             }
             if (j == w.nb[t] - 1) mma_commit(bar(L::kOFull + t));
             if (j + 1 < w.nb[t]) {

@@ -10,19 +10,28 @@
 
 namespace attn {
 
-// K-major operand (reduction dim contiguous): rows start at `tile_addr`
-// (which may point at a row offset that is a multiple of 8 inside the tile);
-// step k16 selects 16 values of the reduction dimension.
-__device__ __forceinline__ uint64_t kmajor_desc16(uint32_t tile_addr, int k16) {
-  const uint32_t addr = tile_addr + (uint32_t)(k16 >> 2) * 16384u + (uint32_t)(k16 & 3) * 32u;
-  return sdesc_sw128(addr, 16, 1024);
+// Cheap K-step addressing for the MMA issuer.  A single thread issues every
+// tcgen05.mma of a CTA, so building descriptors from scratch per instruction
+// (masking, shifting, OR-ing 64-bit fields) costs more issue cycles than the
+// tensor core needs to execute an N=128 MMA.  Instead the issuer builds one
+// base descriptor per tile and adds a compile-time byte offset >> 4 to the
+// start-address field (bits 0-13; shared-memory addresses stay below 256 KB,
+// so the field cannot carry into the neighbouring bits).
+__device__ __forceinline__ uint64_t desc_plus(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
 }
-
-// MN-major operand (the non-reduction dim contiguous, e.g. V as the B operand
-// of P V): 8-row groups along the reduction dim are 1024 B apart (SBO), the
-// 64-value column halves 16 KB apart (LBO); step k16 advances 16 rows.
-__device__ __forceinline__ uint64_t mnmajor_desc16(uint32_t tile_addr, int k16) {
-  return sdesc_sw128(tile_addr + (uint32_t)k16 * 2048u, 16384, 1024);
+// K-major 16-bit tile: byte offset of reduction step k16 (16 values).
+__host__ __device__ constexpr uint32_t kmajor16_off(int k16) {
+  return (uint32_t)(k16 >> 2) * 16384u + (uint32_t)(k16 & 3) * 32u;
+}
+// MN-major 16-bit tile: byte offset of reduction step k16 (16 rows).
+__host__ __device__ constexpr uint32_t mnmajor16_off(int k16) { return (uint32_t)k16 * 2048u; }
+// Base descriptors (K-step 0).
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile_addr) {
+  return sdesc_sw128(tile_addr, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mnmajor_base(uint32_t tile_addr) {
+  return sdesc_sw128(tile_addr, 16384, 1024);
 }
 
 // Snake order over a persistent grid of G CTAs: round k gives CTA c the work
