@@ -48,6 +48,38 @@ COMPONENTS = ("fwd", "bwd", "quant", "fwd_fp8")
 LAUNCHES = {"fwd": 1, "bwd": 3, "quant": 3, "fwd_fp8": 1}  # kernels per component call
 
 
+# Sources whose hash identifies the kernel an ncu traffic figure was taken on.
+KERNEL_SOURCES = {
+    "fwd": ["fwd.cu", "fwd.cuh", "sm103_ptx.cuh", "tiles.cuh"],
+    "fwd_fp8": ["fwd.cu", "fwd.cuh", "sm103_ptx.cuh", "tiles.cuh"],
+    "bwd": ["bwd.cu", "bwd.cuh", "sm103_ptx.cuh", "tiles.cuh"],
+    "quant": ["fp8.cu", "fp8.cuh", "sm103_ptx.cuh"],
+}
+
+
+def sources_sha256(component):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[component]:
+        with open(os.path.join(ROOT, "exact_attention_75_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(component):
+    """DRAM bytes per launch of the component's main kernel from the committed
+    ncu summary (profiles/traffic.json), or None when the kernel's sources have
+    changed since that capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(component)
+    except Exception:
+        return None
+    if not rec or rec.get("sources_sha256") != sources_sha256(component):
+        return None
+    return rec.get("dram_bytes")
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -409,13 +441,13 @@ def main():
         if dom == "fwd_fp8":
             peak = 2 * peaks["bf16_tflops"]  # E4M3 dense = 2x bf16 (nominal ratio)
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": measured_traffic(dom),
                 "peak_kind": f"{peaks['source']} bf16 burst"}
     else:
         ach = r["nbytes"][dom] / (per[dom] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None}
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(dom)}
     line = {"metric": "attention fwd/bwd TFLOP/s", "value": round(value, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(r["ms_step"], 4), "higher_is_better": True, "scaling": "weak",
