@@ -377,10 +377,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           g0 = vsc[b0] / sv_max;
           g1 = vsc[b1] / sv_max;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) {
+            const float2 f = c < 2 ? make_float2(f0, f0) : make_float2(f1, f1);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              s[c * 32 + i] = __uint_as_float(sr[c][i]) * (c < 2 ? f0 : f1);
+            for (int i = 0; i < 16; ++i) {
+              const float2 v = __fmul2_rn(
+                  make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), f);
+              s[c * 32 + 2 * i] = v.x;
+              s[c * 32 + 2 * i + 1] = v.y;
+            }
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -395,18 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
-        // Row max as 8 independent chains (a single 128-long fmaxf chain is
-        // latency-bound).
-        float mx8[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) mx8[c] = s[c];
-#pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-#pragma unroll
-        for (int c = 4; c > 0; c >>= 1)
-#pragma unroll
-          for (int e = 0; e < c; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + c]);
-        const float mx = mx8[0];
+        const float mx = row_max128(s);
         const float m_blk = FP8 ? mx : mx * sl2;
         if (j == 0) {
           m = m_blk;
@@ -436,46 +431,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float mref = (m == -INFINITY) ? 0.f : m;
-        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
+        // Exponent arguments, row sums and scalings run two lanes per
+        // instruction (packed fp32); four partial sums keep the adds independent.
+        const float2 nm2 = make_float2(-mref, -mref);
+        float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
         if constexpr (FP8) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
+            const float2 g2 = c == 0 ? make_float2(g0, g0) : make_float2(g1, g1);
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float pv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int col = c * 64 + 4 * i + e;
-                pv[e] = ex2_approx(s[col] - mref);
-                rs[(4 * i + e) & 7] += pv[e];
-                pv[e] *= (c == 0 ? g0 : g1);
-              }
-              pk[i] = (uint32_t)pack_e4m3x2(pv[0], pv[1]) |
-                      ((uint32_t)pack_e4m3x2(pv[2], pv[3]) << 16);
+              const int col = c * 64 + 4 * i;
+              const float2 x01 = __fadd2_rn(make_float2(s[col], s[col + 1]), nm2);
+              const float2 x23 = __fadd2_rn(make_float2(s[col + 2], s[col + 3]), nm2);
+              float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+              float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+              rs2[(2 * i) & 3] = __fadd2_rn(rs2[(2 * i) & 3], p01);
+              rs2[(2 * i + 1) & 3] = __fadd2_rn(rs2[(2 * i + 1) & 3], p23);
+              p01 = __fmul2_rn(p01, g2);
+              p23 = __fmul2_rn(p23, g2);
+              pk[i] = (uint32_t)pack_e4m3x2(p01.x, p01.y) |
+                      ((uint32_t)pack_e4m3x2(p23.x, p23.y) << 16);
             }
             tmem_st16(s_addr + c * 16, pk);
           }
         } else {
+          const float2 sc2 = make_float2(sl2, sl2);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
-              const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
-              rs[(2 * i) & 7] += p0;
-              rs[(2 * i + 1) & 7] += p1;
+              const float2 x =
+                  __ffma2_rn(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2, nm2);
+              const float p0 = ex2_approx(x.x);
+              const float p1 = ex2_approx(x.y);
+              rs2[i & 3] = __fadd2_rn(rs2[i & 3], make_float2(p0, p1));
               pk[i] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
             }
             tmem_st16(s_addr + c * 16, pk);
           }
         }
-#pragma unroll
-        for (int c = 4; c > 0; c >>= 1)
-#pragma unroll
-          for (int e = 0; e < c; ++e) rs[e] += rs[e + c];
-        l += rs[0];
+        const float2 rsum = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+        l += rsum.x + rsum.y;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::kPFull + t));

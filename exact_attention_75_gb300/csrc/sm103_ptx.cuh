@@ -364,6 +364,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Largest of three (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// Row maximum of 128 values in four independent three-input chains.
+__device__ __forceinline__ float row_max128(const float* s) {
+  float mx[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) mx[e] = fmax3(s[3 * e], s[3 * e + 1], s[3 * e + 2]);
+#pragma unroll
+  for (int c = 12; c < 124; c += 8)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mx[e] = fmax3(mx[e], s[c + 2 * e], s[c + 2 * e + 1]);
+  mx[0] = fmax3(mx[0], s[124], s[125]);
+  mx[1] = fmax3(mx[1], s[126], s[127]);
+  return fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
