@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Watchdog dw = wd;
       volatile int never = 0;
       dw.abort_flag = &never;
+      dw.limit_ns = drain_limit_ns(wd.limit_ns);
       if (kv_it > 0) mbar_wait(bar(L::kKvFull), (kv_it - 1) & 1, dw, 23);
       const uint32_t first = st_it > 2u ? st_it - 2 : 0u;
       for (uint32_t it = first; it < st_it; ++it)
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Watchdog dw = wd;
       volatile int never = 0;
       dw.abort_flag = &never;
+      dw.limit_ns = drain_limit_ns(wd.limit_ns);
       mbar_wait(bar(L::kDrain), 0, dw, 30);
     }
     __syncwarp();

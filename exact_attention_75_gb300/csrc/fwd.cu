@@ -46,9 +46,12 @@ namespace attn {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpRelay = 10;
+// Named barriers (0 is __syncthreads): issuer <-> relay, issuer <-> softmax t.
+constexpr uint32_t kBarKv = 1, kBarP = 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
 constexpr int kPrecF16 = 0, kPrecBF16 = 1, kPrecE4M3 = 2;
 
@@ -60,7 +63,7 @@ struct FwdLayout {
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kSlots * kTileBytes;
   // barrier indices
-  static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8, kDrain = 10;
+  static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kOFull = 8, kDrain = 10;
   static constexpr int kKvFull = 11, kKvEmpty = 11 + kSlots;
   static constexpr int kNumBars = 11 + 2 * kSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -124,7 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kQFull + t), 1);
       mbar_init(bar(L::kQEmpty + t), 1);
       mbar_init(bar(L::kSFull + t), 1);
-      mbar_init(bar(L::kPFull + t), 128);
       mbar_init(bar(L::kOFull + t), 1);
     }
     mbar_init(bar(L::kDrain), 1);
@@ -203,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Watchdog dw = wd;
       volatile int never = 0;
       dw.abort_flag = &never;
+      dw.limit_ns = drain_limit_ns(wd.limit_ns);
       const uint32_t first = kv_it > (uint32_t)L::kSlots ? kv_it - L::kSlots : 0u;
       for (uint32_t it = first; it < kv_it; ++it)
         mbar_wait(bar(L::kKvFull + it % L::kSlots), (it / L::kSlots) & 1, dw, 3);
@@ -210,111 +213,170 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_it[t] > 0) mbar_wait(bar(L::kQFull + t), (q_it[t] - 1) & 1, dw, 4);
     }
     __syncwarp();
+  } else if (warp == kWarpRelay) {
+    // ---------------------------------------------------------- TMA relay ---
+    // Waits for the TMA completions the issuer needs and meets the issuer at
+    // named barrier kBarKv, so that the issuer itself never touches an
+    // mbarrier between its commits (a shared-memory wait there stalls the
+    // tensor pipe).  Schedule, per unit: [Q tiles + K_0], then per block j:
+    // [V_j + K_{j+1}].  After an abort the schedule is still walked to the end
+    // (waits skipped) so every rendezvous pairs up exactly as in a clean run.
+    uint32_t kv_it = 0, q_it[2] = {0, 0};
+    bool aborted = false;
+    auto kv_ready = [&]() {
+      const uint32_t slot = kv_it % L::kSlots;
+      const uint32_t par = (kv_it / L::kSlots) & 1;
+      ++kv_it;
+      if (aborted) return;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvFull + slot), par, wd, 7));
+      aborted = !ok;
+    };
+    for (int k = 0;; ++k) {
+      const int u = snake_unit(k, cta, G);
+      if (u >= p.num_units) break;
+      const Unit w = decode_unit<CAUSAL>(u, p);
+      const int nbmax = max(w.nb[0], w.nb[1]);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (w.nb[t] == 0) continue;
+        const uint32_t par = q_it[t] & 1;
+        ++q_it[t];
+        if (aborted) continue;
+        aborted = !__all_sync(0xffffffffu, mbar_wait(bar(L::kQFull + t), par, wd, 5));
+      }
+      kv_ready();
+      aborted = named_bar_or(kBarKv, 64, aborted);
+      for (int j = 0; j < nbmax; ++j) {
+        kv_ready();
+        if (j + 1 < nbmax) kv_ready();
+        aborted = named_bar_or(kBarKv, 64, aborted);
+      }
+    }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------- tcgen05 issuer ---
-    if (lane == 0) {
-      constexpr uint32_t kIdS =
-          FP8 ? idesc_e4m3(128, 128, false, false) : idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t kIdO =
-          FP8 ? idesc_e4m3(128, D, false, false) : idesc_f16(128, D, BF16, false, true);
-      uint32_t kv_it = 0, q_it[2] = {0, 0}, p_it[2] = {0, 0};
-      bool ok = true;
-      // Base descriptors of the two Q tiles (K-major); K-steps add constants.
-      const uint64_t qdesc[2] = {kmajor_base(sbase + L::kQOff),
-                                 kmajor_base(sbase + L::kQOff + L::kTileBytes)};
-      // S_t = Q_t K^T into tensor-memory columns [128t, 128t+128).
-      auto issue_s = [&](int t, uint32_t kaddr) {
-        const uint64_t kd = kmajor_base(kaddr);
-        const uint64_t qd = t ? qdesc[1] : qdesc[0];
-        const uint32_t dcol = tbase + 128 * t;
-        if constexpr (FP8) {
+    // The whole warp walks the schedule (named barriers count warps); lane 0
+    // issues.  Readiness arrives only through named barriers: kBarKv from the
+    // relay, kBarP + t from softmax warpgroup t.  The OR carried by those
+    // barriers tells the issuer to stop issuing after an abort.
+    constexpr uint32_t kIdS =
+        FP8 ? idesc_e4m3(128, 128, false, false) : idesc_f16(128, 128, BF16, false, false);
+    constexpr uint32_t kIdO =
+        FP8 ? idesc_e4m3(128, D, false, false) : idesc_f16(128, D, BF16, false, true);
+    uint32_t kv_it = 0;
+    bool aborted = false;
+    bool issued = false;
+    // Base descriptors of the two Q tiles (K-major); K-steps add constants.
+    const uint64_t qdesc0 = kmajor_base(sbase + L::kQOff);
+    const uint64_t qdesc1 = kmajor_base(sbase + L::kQOff + L::kTileBytes);
+    // S_t = Q_t K^T into tensor-memory columns [128t, 128t+128).
+    auto issue_s = [&](int t, uint32_t kaddr) {
+      const uint64_t kd = kmajor_base(kaddr);
+      const uint64_t qd = t ? qdesc1 : qdesc0;
+      const uint32_t dcol = tbase + 128 * t;
+      if constexpr (FP8) {
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk)
-            mma_f8_ss(dcol, desc_plus(qd, 32 * kk), desc_plus(kd, 32 * kk), kIdS, kk > 0);
-        } else {
+        for (int kk = 0; kk < D / 32; ++kk)
+          mma_f8_ss(dcol, desc_plus(qd, 32 * kk), desc_plus(kd, 32 * kk), kIdS, kk > 0);
+      } else {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_f16_ss(dcol, desc_plus(qd, kmajor16_off(kk)), desc_plus(kd, kmajor16_off(kk)),
-                       kIdS, kk > 0);
-        }
-      };
-      for (int k = 0; ok; ++k) {
-        const int u = snake_unit(k, cta, G);
-        if (u >= p.num_units) break;
-        const Unit w = decode_unit<CAUSAL>(u, p);
-        const int nbmax = max(w.nb[0], w.nb[1]);
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (w.nb[t] == 0) continue;
-          ok = mbar_wait(bar(L::kQFull + t), q_it[t] & 1, wd, 5);
-          ++q_it[t];
-        }
-        if (!ok) break;
-        // S_t(0) = Q_t K_0^T for both tiles.
-        uint32_t kslot = kv_it % L::kSlots;
-        ok = mbar_wait(bar(L::kKvFull + kslot), (kv_it / L::kSlots) & 1, wd, 6);
-        if (!ok) break;
-        ++kv_it;
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_f16_ss(dcol, desc_plus(qd, kmajor16_off(kk)), desc_plus(kd, kmajor16_off(kk)),
+                     kIdS, kk > 0);
+      }
+    };
+    // O_t += P_t V_j  (A = P from tensor memory)
+    auto issue_pv = [&](int t, uint32_t vaddr, uint32_t acc0) {
+      const uint32_t ocol = tbase + 256 + D * t;
+      const uint32_t pcol = tbase + 128 * t;
+      if constexpr (FP8) {
+        const uint64_t vd = kmajor_base(vaddr);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // 32 keys per MMA
+          mma_f8_ts(ocol, pcol + kk * 8, desc_plus(vd, 32 * kk), kIdO, kk > 0 ? 1u : acc0);
+      } else {
+        const uint64_t vd = mnmajor_base(vaddr);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA
+          mma_f16_ts(ocol, pcol + kk * 8, desc_plus(vd, mnmajor16_off(kk)), kIdO,
+                     kk > 0 ? 1u : acc0);
+      }
+    };
+    for (int k = 0;; ++k) {
+      const int u = snake_unit(k, cta, G);
+      if (u >= p.num_units) break;
+      const Unit w = decode_unit<CAUSAL>(u, p);
+      const int nb0 = w.nb[0], nb1 = w.nb[1];
+      const int nbmax = max(nb0, nb1);
+      // Q tiles and K_0 are in shared memory: S_t(0) = Q_t K_0^T.
+      aborted = named_bar_or(kBarKv, 64, aborted);
+      uint32_t kslot = kv_it % L::kSlots;
+      ++kv_it;
+      if (!aborted) {
         tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (w.nb[t] == 0) continue;
-          issue_s(t, sbase + L::kKvOff + kslot * L::kTileBytes);
-          mma_commit(bar(L::kSFull + t));
-          if (w.nb[t] == 1) mma_commit(bar(L::kQEmpty + t));
-        }
-        mma_commit(bar(L::kKvEmpty + kslot));
-        for (int j = 0; j < nbmax && ok; ++j) {
-          const uint32_t vslot = kv_it % L::kSlots;
-          ok = mbar_wait(bar(L::kKvFull + vslot), (kv_it / L::kSlots) & 1, wd, 7);
-          if (!ok) break;
-          ++kv_it;
-          const bool have_next = j + 1 < nbmax;
-          if (have_next) {
-            kslot = kv_it % L::kSlots;
-            ok = mbar_wait(bar(L::kKvFull + kslot), (kv_it / L::kSlots) & 1, wd, 8);
-            if (!ok) break;
-            ++kv_it;
-          }
-          const uint32_t vaddr = sbase + L::kKvOff + vslot * L::kTileBytes;
+        if (lane == 0) {
           const uint32_t kaddr = sbase + L::kKvOff + kslot * L::kTileBytes;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= w.nb[t]) continue;
-            ok = mbar_wait(bar(L::kPFull + t), p_it[t] & 1, wd, 9);
-            if (!ok) break;
-            ++p_it[t];
-            tc_fence_after();
-            // O_t += P_t V_j  (A = P from tensor memory)
-            const uint32_t ocol = tbase + 256 + D * t;
-            const uint32_t pcol = tbase + 128 * t;
-            const uint32_t acc0 = j > 0 ? 1u : 0u;
-            if constexpr (FP8) {
-              const uint64_t vd = kmajor_base(vaddr);
+          if (nb0 > 0) {
+            issue_s(0, kaddr);
+            mma_commit(bar(L::kSFull + 0));
+            if (nb0 == 1) mma_commit(bar(L::kQEmpty + 0));
+          }
+          if (nb1 > 0) {
+            issue_s(1, kaddr);
+            mma_commit(bar(L::kSFull + 1));
+            if (nb1 == 1) mma_commit(bar(L::kQEmpty + 1));
+          }
+          mma_commit(bar(L::kKvEmpty + kslot));
+        }
+        issued = true;
+        __syncwarp();
+      }
+      for (int j = 0; j < nbmax; ++j) {
+        // V_j and (if any) K_{j+1} are in shared memory.
+        aborted = named_bar_or(kBarKv, 64, aborted);
+        const uint32_t vslot = kv_it % L::kSlots;
+        ++kv_it;
+        const bool have_next = j + 1 < nbmax;
+        if (have_next) {
+          kslot = kv_it % L::kSlots;
+          ++kv_it;
+        }
+        const uint32_t vaddr = sbase + L::kKvOff + vslot * L::kTileBytes;
+        const uint32_t kaddr = sbase + L::kKvOff + kslot * L::kTileBytes;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)  // 32 keys per MMA
-                mma_f8_ts(ocol, pcol + kk * 8, desc_plus(vd, 32 * kk), kIdO, kk > 0 ? 1u : acc0);
-            } else {
-              const uint64_t vd = mnmajor_base(vaddr);
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA
-                mma_f16_ts(ocol, pcol + kk * 8, desc_plus(vd, mnmajor16_off(kk)), kIdO,
-                           kk > 0 ? 1u : acc0);
-            }
-            if (j == w.nb[t] - 1) mma_commit(bar(L::kOFull + t));
-            if (j + 1 < w.nb[t]) {
+        for (int t = 0; t < 2; ++t) {
+          const int nbt = t ? nb1 : nb0;
+          if (j >= nbt) continue;
+          // P_t(j) is in tensor memory.
+          aborted = named_bar_or(kBarP + t, 160, aborted);
+          if (aborted) continue;
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv(t, vaddr, j > 0 ? 1u : 0u);
+            if (j == nbt - 1) mma_commit(bar(L::kOFull + t));
+            if (j + 1 < nbt) {
               issue_s(t, kaddr);
               mma_commit(bar(L::kSFull + t));
-              if (j + 1 == w.nb[t] - 1) mma_commit(bar(L::kQEmpty + t));
+              if (j + 1 == nbt - 1) mma_commit(bar(L::kQEmpty + t));
             }
           }
-          if (!ok) break;
-          mma_commit(bar(L::kKvEmpty + vslot));
-          if (have_next) mma_commit(bar(L::kKvEmpty + kslot));
+          __syncwarp();
+        }
+        if (!aborted) {
+          if (lane == 0) {
+            mma_commit(bar(L::kKvEmpty + vslot));
+            if (have_next) mma_commit(bar(L::kKvEmpty + kslot));
+          }
+          __syncwarp();
         }
       }
-      // Drain: wait until every MMA issued above has completed.
+    }
+    // Drain: wait until every MMA issued above has completed.
+    if (lane == 0 && issued) {
       mma_commit(bar(L::kDrain));
       Watchdog dw = wd;
       volatile int never = 0;
       dw.abort_flag = &never;
+      dw.limit_ns = drain_limit_ns(wd.limit_ns);
       mbar_wait(bar(L::kDrain), 0, dw, 10);
     }
     __syncwarp();
@@ -327,8 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tbase + lane_base + 256u + D * t;
     const float sl2 = p.scale_log2;
     uint32_t s_it = 0, o_it = 0;
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
+    // After an abort the schedule is still walked to the end with every wait
+    // and all tensor-memory work skipped, so the issuer's named barriers
+    // always pair up.
+    bool aborted = false;
+    for (int k = 0;; ++k) {
       const int u = snake_unit(k, cta, G);
       if (u >= p.num_units) break;
       const Unit w = decode_unit<CAUSAL>(u, p);
@@ -356,10 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         sv_max = mv > 0.f ? mv : 1.f;
       }
       for (int j = 0; j < nb; ++j) {
-        ok = mbar_wait(bar(L::kSFull + t), s_it & 1, wd, 11);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+        const uint32_t spar = s_it & 1;
         ++s_it;
+        if (!aborted)
+          aborted = !__all_sync(0xffffffffu, mbar_wait(bar(L::kSFull + t), spar, wd, 11));
+        if (!aborted) {
         tc_fence_after();
         uint32_t sr[4][32];
 #pragma unroll
@@ -478,14 +544,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += rsum.x + rsum.y;
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(L::kPFull + t));
+        }
+        // Hand P_t(j) to the issuer (and learn whether anyone has aborted).
+        aborted = named_bar_or(kBarP + t, 160, aborted);
       }
-      if (!ok) break;
       // ------------------------------------------------------- epilogue ---
-      ok = mbar_wait(bar(L::kOFull + t), o_it & 1, wd, 12);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      const uint32_t opar = o_it & 1;
       ++o_it;
+      if (!aborted)
+        aborted = !__all_sync(0xffffffffu, mbar_wait(bar(L::kOFull + t), opar, wd, 12));
+      if (aborted) continue;
       tc_fence_after();
       const float inv_l = (FP8 ? sv_max : 1.0f) / l;
       const size_t grow = (size_t)w.bh * p.N + row;

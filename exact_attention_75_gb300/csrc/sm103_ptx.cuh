@@ -84,6 +84,14 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
+// Limit for a drain wait (one that only waits for MMAs or copies this thread
+// already issued, before shared or tensor memory is released): never below
+// one second, whatever limit the caller configured, so a small configured
+// limit cannot free memory that is still being written.
+__device__ __forceinline__ uint64_t drain_limit_ns(uint64_t limit_ns) {
+  return limit_ns > 1000000000ull ? limit_ns : 1000000000ull;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false if
 // the time limit ran out or another role in the CTA has aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Watchdog& wd,
@@ -149,6 +157,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Named barrier over `count` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also returns the OR of `pred` over the participating
+// threads (a rendezvous that carries an abort bit both ways).
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // Named barrier that also returns the AND of `pred` over the participating

@@ -21,3 +21,36 @@ def test_wait_timeout_is_reported_and_context_survives(attn_lib):
     torch.cuda.synchronize()
     assert attn_lib.poll_status()[0] == 0
     assert torch.isfinite(o.float()).all()
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
+def test_forward_winds_down_when_waits_run_out(attn_lib, dtype, d):
+    """With a 1 us wait limit, pipeline waits inside the forward kernel run out
+    during an ordinary launch.  Every role must then walk the rest of its
+    schedule without waiting (the issuer's named barriers still pair up), the
+    kernel must end with ATTN_ERR_TIMEOUT in the status word, and the next
+    launch at the normal limit must be correct."""
+    import numpy as np
+    import oracle
+    from helpers import to64
+    w = wl.Workload("t", "fwd", 2, 4, 2048, d, dtype, True, seed=d)
+    inp = wl.make_inputs(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    attn_lib.poll_status()
+    attn_lib.set_wait_limit_us(1)
+    try:
+        attn_lib.fwd(q, k, v, causal=True)
+        st, detail = attn_lib.poll_status()
+    finally:
+        attn_lib.set_wait_limit_us(0)  # back to the default limit
+    # 4 = ATTN_ERR_TIMEOUT; 0 only if no wait happened to outlive 1 us
+    assert st in (0, 4), (st, hex(detail))
+    if st == 4:
+        assert (detail & 0xFF) == 4
+    o, lse = attn_lib.fwd(q, k, v, causal=True)
+    assert attn_lib.poll_status() == (0, 0)
+    rows = np.arange(0, w.N, 97)
+    O_ref, L_ref = oracle.attention_rows(to64(inp["q"][1, 2]), to64(inp["k"][1, 2]),
+                                         to64(inp["v"][1, 2]), rows, True, w.scale)
+    assert np.max(np.abs(to64(o[1, 2])[rows] - O_ref)) <= 2e-2
+    assert np.max(np.abs(to64(lse[1, 2])[rows] - L_ref)) <= 5e-3
