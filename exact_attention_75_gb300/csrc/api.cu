@@ -187,9 +187,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (!shape_ok(B, H, N, d)) return 0;
   const size_t rows = (size_t)B * H * N;
-  const size_t dbytes = (rows * 4 + 255) & ~(size_t)255;
-  const size_t qbytes = (rows * d * 4 + 255) & ~(size_t)255;
-  return dbytes + qbytes;
+  return (rows * 4 + 255) & ~(size_t)255;  // D = rowsum(dO o O), fp32
 }
 
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -220,8 +218,6 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
       !encode_3d(&a.tmV, v, dt, 2, d, N, BH, 64, 128) ||
       !encode_3d(&a.tmDO, dout, dt, 2, d, N, BH, 64, 128))
     return ATTN_ERR_CUDA;
-  const size_t rows = (size_t)BH * N;
-  const size_t dbytes = (rows * 4 + 255) & ~(size_t)255;
   BwdParams& p = a.params;
   p.q = q;
   p.k = k;
@@ -233,10 +229,6 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   p.dk = dk;
   p.dv = dv;
   p.delta = static_cast<float*>(workspace);
-  p.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dbytes);
-  if (!encode_3d(&a.tmDQacc, p.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, BH, 128, 32,
-                 CU_TENSOR_MAP_SWIZZLE_NONE))
-    return ATTN_ERR_CUDA;
   p.status = di->status;
   p.BH = (int)BH;
   p.N = N;

@@ -3,30 +3,33 @@
 // "FlashAttention-2: Faster Attention with Better Parallelism and Work
 // Partitioning" (review page), "Methods" and "핵심 구성요소": the forward pass
 // keeps only the log-sum-exp, and the backward pass recomputes P from it
-// instead of storing the N x N matrix.  The backward kernel of "Triton 07:
-// Flash Attention v3" is a three-stage one; here the three stages are
-//   1. bwd_pre_kernel   D_i = sum_c dO_ic O_ic (warp-shuffle row reduction),
-//                       and the fp32 dQ accumulator is zeroed;
-//   2. bwd_main_kernel  one CTA per 128-key K/V tile (persistent, longest
-//                       first): for every 128-query tile i it recomputes
-//                       S^T = K Q_i^T and P^T = exp2(S^T c - LSE_i log2 e),
-//                       dP^T = V dO_i^T, dS^T = P^T o (dP^T - D_i), and
-//                       accumulates dV += P^T dO_i, dK += dS^T Q_i in tensor
-//                       memory; dQ_i^T = K^T dS^T is drained into the fp32
-//                       accumulator with TMA bulk reduce-adds;
-//   3. bwd_post_kernel  dQ = scale * dQ_acc, rounded to 16 bit.
+// instead of storing the N x N matrix.  The backward of "Triton 07: Flash
+// Attention v3" is staged; here the stages are
+//   1. bwd_pre_kernel  D_i = sum_c dO_ic O_ic (warp-shuffle row reduction);
+//   2. bwd_dkv_kernel  one CTA per 128-key K/V tile (persistent, longest
+//                      first): for every 128-query tile i it recomputes
+//                      S^T = K Q_i^T and P^T = exp2(S^T c - LSE_i log2 e),
+//                      dP^T = V dO_i^T, dS^T = P^T o (dP^T - D_i), and
+//                      accumulates dV += P^T dO_i, dK += dS^T Q_i in tensor
+//                      memory;
+//   3. bwd_dq_kernel   one CTA per 128-query tile: for every key tile j it
+//                      recomputes S = Q K_j^T, P, dP = dO V_j^T and dS and
+//                      accumulates dQ += dS K_j in tensor memory.
+// Splitting dQ from dK/dV recomputes S and dP once more (7 instead of 5
+// matrix products) but removes the cross-CTA reduction of dQ: with it, each
+// step also had to stage 64 KB of fp32 partial dQ through shared memory for
+// a TMA reduce-add, and shared-memory bandwidth (128 B/clock/SM, all of it
+// taken by an N = 128 MMA with both operands in shared memory) is what
+// bounds these kernels.  Every MMA here has N = 128 and keeps its
+// accumulator in tensor memory; P and dS feed the dV / dK / dQ products
+// from tensor memory.
 //
-// Main-kernel CTA organisation (320 threads):
-//   warps 0-3 / 4-7  compute warpgroups for query columns [0,64) / [64,128)
-//                    of each step; thread = key row of the tile (TMEM lane)
-//   warp 8           producer: TMA for K, V (once per unit) and Q_i, dO_i
-//                    (2-stage ring); LSE*log2(e) and D for the 128 queries
+// CTA organisation of both kernels (320 threads):
+//   warps 0-3 / 4-7  compute warpgroups, one per half of the 128 columns of
+//                    S (query columns in bwd_dkv, key columns in bwd_dq);
+//                    thread = TMEM lane = row
+//   warp 8           TMA producer
 //   warp 9           tcgen05 issuer + tensor-memory owner
-// Tensor memory: dV [0,128)  dK [128,256)  S^T_0 [256,320)  dP^T_0 [320,384)
-//                S^T_1 [384,448)  dP^T_1 [448,512); P^T_h and dS^T_h (16-bit)
-//                overwrite the first 32 columns of S^T_h / dP^T_h, and
-//                dQ^T_h (fp32, 64 columns) reuses the S^T_h columns once the
-//                dV MMA has consumed P^T_h.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -45,37 +48,63 @@ constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStatusLayout = 5;  // shared memory not 1024-byte aligned
+constexpr int kTile = 32768;           // 128 x 128 16-bit values
 
-struct BwdLayout {
-  static constexpr int kTile = 32768;             // 128 x 128 16-bit values
+// Column of the K-step kk (16 values of the contraction index) of a 16-bit
+// operand that the two warpgroups wrote into the first 32 columns of their
+// 64-column halves of a 128-column tensor-memory region.
+__device__ __forceinline__ uint32_t half_packed_col(int kk) {
+  return kk < 4 ? 8u * kk : 64u + 8u * (kk - 4);
+}
+
+__device__ __forceinline__ uint32_t pack16x2(bool bf16, float lo, float hi) {
+  return bf16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+
+// Loads a 128 x 128 16-bit tile (two 64-column boxes) with TMA.
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                          int row0, int bh) {
+  tma_load_3d(dst, map, bar, 0, row0, bh);
+  tma_load_3d(dst + 16384, map, bar, 64, row0, bh);
+}
+
+// ============================================================ dK, dV kernel ===
+
+// Per step s the tensor core runs S^T(s) | dK(s-1) | dP^T(s) | dV(s), so the
+// warpgroups' P^T(s) overlaps dK(s-1) and dP^T(s), and their dS^T(s)
+// overlaps dV(s) and S^T(s+1).  Q_i is then read until the next step (by
+// dK), so Q has a ring of 3 slots; dO_i and the -LSE / -D vectors of its
+// queries have one of 2 slots.
+struct DkvLayout {
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
-  static constexpr int kStage0 = 2 * kTile;       // stage s: Q_i then dO_i
-  static constexpr int kStageBytes = 2 * kTile;
-  static constexpr int kStages = 2;
-  static constexpr int kDS = kStage0 + kStages * kStageBytes;  // dS^T halves, 16 KB each
-  static constexpr int kVec = kDS + 2 * 16384;    // per stage: LSE2[128], D[128]
-  static constexpr int kBar = kVec + kStages * 1024;
+  static constexpr int kQSlots = 3, kDoSlots = 2;
+  static constexpr int kQ0 = 2 * kTile;
+  static constexpr int kDo0 = kQ0 + kQSlots * kTile;
+  static constexpr int kVec = kDo0 + kDoSlots * kTile;  // per dO slot: -LSE2[128], -D[128]
+  static constexpr int kBar = kVec + kDoSlots * 1024;
   enum {
-    kKvFull, kKvEmpty, kQFull, kQFull1, kQEmpty, kQEmpty1, kSFull, kSFull1, kPFull, kPFull1,
-    kDqFull, kDqFull1, kDqFree, kDqFree1, kDkvFull, kDkvFree, kDrain, kNumBars
+    kKvFull, kKvEmpty, kQFull, kQEmpty = kQFull + kQSlots, kDoFull = kQEmpty + kQSlots,
+    kDoEmpty = kDoFull + kDoSlots, kSFull = kDoEmpty + kDoSlots, kDpFull, kPReady, kDsReady,
+    kDkvFull, kDkvFree, kDrain, kNumBars
   };
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static_assert(kBytes <= 232448, "shared memory budget (227 KB) exceeded");
 };
 
-constexpr uint32_t kColDV = 0, kColDK = 128;
-__device__ __forceinline__ uint32_t col_s(int h) { return 256u + 128u * h; }
-__device__ __forceinline__ uint32_t col_dp(int h) { return 320u + 128u * h; }
+// Tensor memory: dV [0,128)  dK [128,256)  S^T [256,384)  dP^T [384,512).
+// P^T (16-bit) of warpgroup h overwrites S^T columns [256+64h, 256+64h+32),
+// dS^T those of dP^T.
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
-struct BwdUnit {
+struct DkvUnit {
   int bh, j, i0, nsteps;
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ BwdUnit decode_bwd_unit(int u, const BwdParams& p) {
-  BwdUnit w;
+__device__ __forceinline__ DkvUnit decode_dkv_unit(int u, const BwdParams& p) {
+  DkvUnit w;
   if (CAUSAL) {
     // K/V tile j sees query tiles j..n-1: ascending j is longest first.
     w.j = u / p.BH;
@@ -92,10 +121,10 @@ __device__ __forceinline__ BwdUnit decode_bwd_unit(int u, const BwdParams& p) {
 
 template <bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
-  using L = BwdLayout;
+    bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                   const BwdParams p) {
+  using L = DkvLayout;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -115,14 +144,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_init(bar(L::kKvFull), 1);
     mbar_init(bar(L::kKvEmpty), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kQFull + s), 2);    // TMA bytes + the LSE/D writer
+    for (int s = 0; s < L::kQSlots; ++s) {
+      mbar_init(bar(L::kQFull + s), 1);
       mbar_init(bar(L::kQEmpty + s), 1);
-      mbar_init(bar(L::kSFull + s), 1);
-      mbar_init(bar(L::kPFull + s), 128);
-      mbar_init(bar(L::kDqFull + s), 1);
-      mbar_init(bar(L::kDqFree + s), 128);
     }
+    for (int s = 0; s < L::kDoSlots; ++s) {
+      mbar_init(bar(L::kDoFull + s), 2);  // TMA bytes + the -LSE/-D writer
+      mbar_init(bar(L::kDoEmpty + s), 1);
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kDpFull), 1);
+    mbar_init(bar(L::kPReady), 256);
+    mbar_init(bar(L::kDsReady), 256);
     mbar_init(bar(L::kDkvFull), 1);
     mbar_init(bar(L::kDkvFree), 256);
     mbar_init(bar(L::kDrain), 1);
@@ -149,19 +182,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmDO);
     }
     uint32_t kv_it = 0, st_it = 0;
+    uint32_t q_issued = 0, do_issued = 0;  // copies issued (lane 0), for the drain
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int u = snake_unit(k, cta, G);
       if (u >= num_units) break;
-      const BwdUnit w = decode_bwd_unit<CAUSAL>(u, p);
+      const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
       if (lane == 0) {
         ok = mbar_wait(bar(L::kKvEmpty), (kv_it & 1) ^ 1, wd, 21);
         if (ok) {
-          mbar_arrive_expect_tx(bar(L::kKvFull), 2 * L::kTile);
-          for (int h = 0; h < 2; ++h) {
-            tma_load_3d(sbase + L::kK + h * 16384, &tmK, bar(L::kKvFull), h * 64, w.j * 128, w.bh);
-            tma_load_3d(sbase + L::kV + h * 16384, &tmV, bar(L::kKvFull), h * 64, w.j * 128, w.bh);
-          }
+          mbar_arrive_expect_tx(bar(L::kKvFull), 2 * kTile);
+          load_tile(sbase + L::kK, &tmK, bar(L::kKvFull), w.j * 128, w.bh);
+          load_tile(sbase + L::kV, &tmV, bar(L::kKvFull), w.j * 128, w.bh);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -169,133 +201,142 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++kv_it;
       for (int s = 0; s < w.nsteps && ok; ++s) {
         const int i = w.i0 + s;
-        const uint32_t stage = st_it & 1;
-        if (lane == 0) ok = mbar_wait(bar(L::kQEmpty + stage), ((st_it >> 1) & 1) ^ 1, wd, 22);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        const uint32_t qaddr = sbase + L::kStage0 + stage * L::kStageBytes;
+        const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(L::kQFull + stage), 2 * L::kTile);
-          for (int h = 0; h < 2; ++h) {
-            tma_load_3d(qaddr + h * 16384, &tmQ, bar(L::kQFull + stage), h * 64, i * 128, w.bh);
-            tma_load_3d(qaddr + L::kTile + h * 16384, &tmDO, bar(L::kQFull + stage), h * 64,
-                        i * 128, w.bh);
+          ok = mbar_wait(bar(L::kQEmpty + qs), ((st_it / L::kQSlots) & 1) ^ 1, wd, 22);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(L::kQFull + qs), kTile);
+            load_tile(sbase + L::kQ0 + qs * kTile, &tmQ, bar(L::kQFull + qs), i * 128, w.bh);
+            ++q_issued;
+            ok = mbar_wait(bar(L::kDoEmpty + ds), ((st_it / L::kDoSlots) & 1) ^ 1, wd, 23);
+          }
+          if (ok) {
+            mbar_arrive_expect_tx(bar(L::kDoFull + ds), kTile);
+            load_tile(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds), i * 128, w.bh);
+            ++do_issued;
           }
         }
-        // LSE * log2(e) and D of the 128 queries (padding rows: +inf / 0, so
-        // their P and dS vanish).
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // -LSE * log2(e) and -D of the 128 queries (padding rows: -inf / 0,
+        // so their P and dS vanish).
         float l2[4], dd[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int q = i * 128 + 4 * lane + e;
           const bool in = q < p.N;
           const size_t g = (size_t)w.bh * p.N + (in ? q : 0);
-          l2[e] = in ? p.lse[g] * kLog2e : INFINITY;
-          dd[e] = in ? p.delta[g] : 0.f;
+          l2[e] = in ? -p.lse[g] * kLog2e : -INFINITY;
+          dd[e] = in ? -p.delta[g] : 0.f;
         }
-        float4* vec = reinterpret_cast<float4*>(smem + L::kVec + stage * 1024);
+        float4* vec = reinterpret_cast<float4*>(smem + L::kVec + ds * 1024);
         vec[lane] = make_float4(l2[0], l2[1], l2[2], l2[3]);
         vec[32 + lane] = make_float4(dd[0], dd[1], dd[2], dd[3]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::kQFull + stage));
+        if (lane == 0) mbar_arrive(bar(L::kDoFull + ds));
         ++st_it;
       }
     }
     if (lane == 0) {
+      // Drain: the copies of the last ring rounds must have landed.
       Watchdog dw = wd;
       volatile int never = 0;
       dw.abort_flag = &never;
       dw.limit_ns = drain_limit_ns(wd.limit_ns);
-      if (kv_it > 0) mbar_wait(bar(L::kKvFull), (kv_it - 1) & 1, dw, 23);
-      const uint32_t first = st_it > 2u ? st_it - 2 : 0u;
-      for (uint32_t it = first; it < st_it; ++it)
-        mbar_wait(bar(L::kQFull + (it & 1)), (it >> 1) & 1, dw, 24);
+      if (kv_it > 0) mbar_wait(bar(L::kKvFull), (kv_it - 1) & 1, dw, 24);
+      for (uint32_t it = q_issued > (uint32_t)L::kQSlots ? q_issued - L::kQSlots : 0u;
+           it < q_issued; ++it)
+        mbar_wait(bar(L::kQFull + it % L::kQSlots), (it / L::kQSlots) & 1, dw, 24);
+      for (uint32_t it = do_issued > (uint32_t)L::kDoSlots ? do_issued - L::kDoSlots : 0u;
+           it < do_issued; ++it)
+        mbar_wait(bar(L::kDoFull + it % L::kDoSlots), (it / L::kDoSlots) & 1, dw, 24);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ tcgen05 issuer ---
+    // Per step s: S^T(s) | dK(s-1) | dP^T(s) | dV(s); after the unit's last
+    // step its dK.
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f16(128, 64, BF16, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_f16(128, 128, BF16, false, true);  // dV, dK
-      constexpr uint32_t kIdQ = idesc_f16(128, 64, BF16, true, true);     // dQ^T
       uint32_t kv_it = 0, st_it = 0, unit_it = 0;
-      uint32_t dq_it[2] = {0, 0}, p_it[2] = {0, 0};
       bool ok = true;
-      // Base descriptors: K and V as K-major A operands of S^T / dP^T, K as
-      // the MN-major A operand of dQ^T, the dS^T halves as MN-major B.
+      // K and V as K-major A operands of S^T / dP^T.
       const uint64_t kd_k = kmajor_base(sbase + L::kK), vd_k = kmajor_base(sbase + L::kV);
-      const uint64_t kd_mn = mnmajor_base(sbase + L::kK);
-      const uint64_t dsd[2] = {mnmajor_base(sbase + L::kDS), mnmajor_base(sbase + L::kDS + 16384)};
+      // dK(s) += dS^T(s) Q_i(s) with Q from its ring slot; then the slots of
+      // step s are free (its dS^T phase, the last reader of its -D, is done).
+      auto issue_dk = [&](uint32_t step, uint32_t acc0) {
+        const uint32_t qs = step % L::kQSlots;
+        const uint64_t qd_mn = mnmajor_base(sbase + L::kQ0 + qs * kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(tbase + kColDK, tbase + kColDP + half_packed_col(kk),
+                     desc_plus(qd_mn, mnmajor16_off(kk)), kIdKV, kk > 0 ? 1u : acc0);
+        mma_commit(bar(L::kQEmpty + qs));
+        mma_commit(bar(L::kDoEmpty + step % L::kDoSlots));
+      };
       for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, G);
         if (u >= num_units) break;
-        const BwdUnit w = decode_bwd_unit<CAUSAL>(u, p);
+        const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
         ok = mbar_wait(bar(L::kKvFull), kv_it & 1, wd, 25);
         if (!ok) break;
         ++kv_it;
         tc_fence_after();
         for (int s = 0; s < w.nsteps && ok; ++s) {
-          const uint32_t stage = st_it & 1;
-          ok = mbar_wait(bar(L::kQFull + stage), (st_it >> 1) & 1, wd, 26);
+          const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
+          const uint32_t par = st_it & 1;
+          ok = mbar_wait(bar(L::kQFull + qs), (st_it / L::kQSlots) & 1, wd, 26);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qaddr = sbase + L::kStage0 + stage * L::kStageBytes;
-          const uint32_t doaddr = qaddr + L::kTile;
-          for (int h = 0; h < 2 && ok; ++h) {
-            if (dq_it[h] > 0) {
-              ok = mbar_wait(bar(L::kDqFree + h), (dq_it[h] - 1) & 1, wd, 27);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            const uint64_t qd = kmajor_base(qaddr + 8192u * h);
-            const uint64_t dod = kmajor_base(doaddr + 8192u * h);
-            const uint32_t cs = tbase + col_s(h), cdp = tbase + col_dp(h);
+          // S^T = K Q_i^T (the previous P^T was consumed by the previous dV,
+          // and its S^T read before that P^T was handed over)
+          const uint64_t qd = kmajor_base(sbase + L::kQ0 + qs * kTile);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(cs, desc_plus(kd_k, kmajor16_off(kk)), desc_plus(qd, kmajor16_off(kk)),
-                         kIdS, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(cdp, desc_plus(vd_k, kmajor16_off(kk)), desc_plus(dod, kmajor16_off(kk)),
-                         kIdS, kk > 0);
-            mma_commit(bar(L::kSFull + h));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tbase + kColS, desc_plus(kd_k, kmajor16_off(kk)),
+                       desc_plus(qd, kmajor16_off(kk)), kIdS, kk > 0);
+          mma_commit(bar(L::kSFull));
+          // dK(s-1): its dS^T must be in tensor memory
+          if (s > 0) {
+            ok = mbar_wait(bar(L::kDsReady), par ^ 1, wd, 27);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dk(st_it - 1, s > 1 ? 1u : 0u);
           }
+          // dP^T = V dO_i^T (dS^T(s-1) in these columns has just been consumed)
+          ok = mbar_wait(bar(L::kDoFull + ds), (st_it / L::kDoSlots) & 1, wd, 28);
           if (!ok) break;
+          tc_fence_after();
+          const uint32_t doaddr = sbase + L::kDo0 + ds * kTile;
+          const uint64_t dod = kmajor_base(doaddr);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tbase + kColDP, desc_plus(vd_k, kmajor16_off(kk)),
+                       desc_plus(dod, kmajor16_off(kk)), kIdS, kk > 0);
+          mma_commit(bar(L::kDpFull));
+          // dV / dK of the previous unit have been stored
           if (s == 0 && unit_it > 0) {
-            ok = mbar_wait(bar(L::kDkvFree), (unit_it - 1) & 1, wd, 28);
+            ok = mbar_wait(bar(L::kDkvFree), (unit_it - 1) & 1, wd, 29);
             if (!ok) break;
-            tc_fence_after();
           }
-          for (int h = 0; h < 2 && ok; ++h) {
-            ok = mbar_wait(bar(L::kPFull + h), p_it[h] & 1, wd, 29);
-            if (!ok) break;
-            ++p_it[h];
-            tc_fence_after();
-            const uint64_t dod_mn = mnmajor_base(doaddr + 8192u * h);
-            const uint64_t qd_mn = mnmajor_base(qaddr + 8192u * h);
-            const uint32_t acc0 = (s > 0 || h > 0) ? 1u : 0u;
-            const uint32_t cs = tbase + col_s(h), cdp = tbase + col_dp(h);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ts(tbase + kColDV, cs + 8 * kk, desc_plus(dod_mn, mnmajor16_off(kk)), kIdKV,
-                         kk > 0 ? 1u : acc0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ts(tbase + kColDK, cdp + 8 * kk, desc_plus(qd_mn, mnmajor16_off(kk)), kIdKV,
-                         kk > 0 ? 1u : acc0);
-            const uint64_t dsb = h ? dsd[1] : dsd[0];
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(cs, desc_plus(kd_mn, mnmajor16_off(kk)), desc_plus(dsb, mnmajor16_off(kk)),
-                         kIdQ, kk > 0);
-            mma_commit(bar(L::kDqFull + h));
-            ++dq_it[h];
-          }
+          // dV += P^T dO_i  (A = P^T from tensor memory)
+          ok = mbar_wait(bar(L::kPReady), par, wd, 30);
           if (!ok) break;
-          mma_commit(bar(L::kQEmpty + stage));
+          tc_fence_after();
+          const uint64_t dod_mn = mnmajor_base(doaddr);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ts(tbase + kColDV, tbase + kColS + half_packed_col(kk),
+                       desc_plus(dod_mn, mnmajor16_off(kk)), kIdKV, kk > 0 || s > 0 ? 1u : 0u);
           ++st_it;
         }
         if (!ok) break;
+        // the unit's last dK, then hand dK / dV to the warpgroups
+        ok = mbar_wait(bar(L::kDsReady), (st_it - 1) & 1, wd, 31);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dk(st_it - 1, w.nsteps > 1 ? 1u : 0u);
         mma_commit(bar(L::kDkvFull));
         mma_commit(bar(L::kKvEmpty));
         ++unit_it;
@@ -305,125 +346,123 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int never = 0;
       dw.abort_flag = &never;
       dw.limit_ns = drain_limit_ns(wd.limit_ns);
-      mbar_wait(bar(L::kDrain), 0, dw, 30);
+      mbar_wait(bar(L::kDrain), 0, dw, 32);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------ compute warpgroups ---
     const int h = warp >> 2;                 // query half of every step
-    const int r = threadIdx.x & 127;         // TMEM lane: key row (or d for dQ^T)
+    const int r = threadIdx.x & 127;         // TMEM lane: key row
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tbase + lane_base + col_s(h);
-    const uint32_t dp_addr = tbase + lane_base + col_dp(h);
-    uint8_t* ds_row = smem + L::kDS + 16384 * h + r * 128;
+    const uint32_t s_addr = tbase + lane_base + kColS + 64 * h;
+    const uint32_t dp_addr = tbase + lane_base + kColDP + 64 * h;
     const float sl2 = p.scale_log2;
-    uint32_t s_it = 0, st_it = 0, unit_it = 0;
+    uint32_t st_it = 0, unit_it = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int u = snake_unit(k, cta, G);
       if (u >= num_units) break;
-      const BwdUnit w = decode_bwd_unit<CAUSAL>(u, p);
+      const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
       for (int s = 0; s < w.nsteps; ++s) {
         const int i = w.i0 + s;
-        const uint32_t stage = st_it & 1;
-        ok = mbar_wait(bar(L::kSFull + h), s_it & 1, wd, 31);
-        ok = ok && mbar_wait(bar(L::kQFull + stage), (st_it >> 1) & 1, wd, 32);
-        // The dS^T buffer doubles as the dQ staging area of the previous
-        // step: its TMA reads must be done before dS^T is written again.
-        if ((threadIdx.x & 127) == 0) bulk_wait_group_read0();
-        // Exit decisions are uniform over the warpgroup: its four warps meet
-        // at named barriers further down.
+        const uint32_t ds = st_it % L::kDoSlots;
+        const uint32_t par = st_it & 1;
+        ok = mbar_wait(bar(L::kSFull), par, wd, 33);
+        // the -LSE / -D vectors travel with dO_i
+        ok = ok && mbar_wait(bar(L::kDoFull + ds), (st_it / L::kDoSlots) & 1, wd, 34);
+        // Exit decisions are uniform over the warpgroup (its warps meet at
+        // named barriers).
         ok = named_bar_and(1 + h, 128, ok);
         if (!ok) break;
-        ++s_it;
         tc_fence_after();
-        const float4* lse4 = reinterpret_cast<const float4*>(smem + L::kVec + stage * 1024) + 16 * h;
-        const float4* d4 = lse4 + 32;
+        const float4* nlse4 = reinterpret_cast<const float4*>(smem + L::kVec + ds * 1024) + 16 * h;
+        const float4* nd4 = nlse4 + 32;
         const bool diag = CAUSAL && (i == w.j);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(s_addr + 32 * c, sr);
-          tmem_ld32(dp_addr + 32 * c, dr);
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        // ---- P^T = exp2(S^T c - LSE log2 e), kept in fp32 for dS^T.  Both
+        // 32-column chunks are loaded before one wait.
+        float pr[64];
+        {
+          uint32_t sa[32], sb[32];
+          tmem_ld32(s_addr, sa);
+          tmem_ld32(s_addr + 32, sb);
           tmem_wait_ld();
-          reg_fence32(sr);
-          reg_fence32(dr);
-          uint32_t pp[16], pd[16];
+          reg_fence32(sa);
+          reg_fence32(sb);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const float4 lq = lse4[8 * c + v];
-            const float4 dq = d4[8 * c + v];
-            const float lv[4] = {lq.x, lq.y, lq.z, lq.w};
-            const float dv[4] = {dq.x, dq.y, dq.z, dq.w};
-            float pv[4], sv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = 32 * c + 4 * v + e;  // query column within the half
-              float pe = ex2_approx(fmaf(__uint_as_float(sr[4 * v + e]), sl2, -lv[e]));
-              if (diag && (64 * h + col) < r) pe = 0.f;
-              pv[e] = pe;
-              sv[e] = pe * (__uint_as_float(dr[4 * v + e]) - dv[e]);
-            }
-            pp[2 * v] = BF16 ? pack_bf16x2(pv[0], pv[1]) : pack_f16x2(pv[0], pv[1]);
-            pp[2 * v + 1] = BF16 ? pack_bf16x2(pv[2], pv[3]) : pack_f16x2(pv[2], pv[3]);
-            pd[2 * v] = BF16 ? pack_bf16x2(sv[0], sv[1]) : pack_f16x2(sv[0], sv[1]);
-            pd[2 * v + 1] = BF16 ? pack_bf16x2(sv[2], sv[3]) : pack_f16x2(sv[2], sv[3]);
+          for (int v = 0; v < 16; ++v) {
+            const uint32_t* src = v < 8 ? sa : sb;
+            const int o = 4 * (v & 7);
+            const float4 nl = nlse4[v];
+            const float2 x01 = __ffma2_rn(
+                make_float2(__uint_as_float(src[o]), __uint_as_float(src[o + 1])), sl2x2,
+                make_float2(nl.x, nl.y));
+            const float2 x23 = __ffma2_rn(
+                make_float2(__uint_as_float(src[o + 2]), __uint_as_float(src[o + 3])), sl2x2,
+                make_float2(nl.z, nl.w));
+            pr[4 * v] = ex2_approx(x01.x);
+            pr[4 * v + 1] = ex2_approx(x01.y);
+            pr[4 * v + 2] = ex2_approx(x23.x);
+            pr[4 * v + 3] = ex2_approx(x23.y);
           }
-          tmem_st16(s_addr + 16 * c, pp);
-          tmem_st16(dp_addr + 16 * c, pd);
-          // dS^T row r, query columns [32c, 32c+32) = 16-byte chunks 4c..4c+3,
-          // stored with the 128-byte swizzle (chunk index xor row % 8).
+          if (diag) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int chunk = 4 * c + v;
-            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
-                make_uint4(pd[4 * v], pd[4 * v + 1], pd[4 * v + 2], pd[4 * v + 3]);
+            for (int col = 0; col < 64; ++col)  // query column within the half
+              if (64 * h + col < r) pr[col] = 0.f;  // query before key
           }
+          uint32_t pp[16], pq[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            pp[e] = pack16x2(BF16, pr[2 * e], pr[2 * e + 1]);
+            pq[e] = pack16x2(BF16, pr[32 + 2 * e], pr[32 + 2 * e + 1]);
+          }
+          tmem_st16(s_addr, pp);
+          tmem_st16(s_addr + 16, pq);
         }
-        fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(L::kPFull + h));
-        // dQ^T_h: TMEM lane = head-dim index r, column = query of this half.
-        ok = mbar_wait(bar(L::kDqFull + h), (s_it - 1) & 1, wd, 33);
+        mbar_arrive(bar(L::kPReady));
+        // ---- dS^T = P^T o (dP^T - D)
+        ok = mbar_wait(bar(L::kDpFull), par, wd, 35);
         ok = named_bar_and(1 + h, 128, ok);
         if (!ok) break;
         tc_fence_after();
-        uint32_t qa[32], qb[32];
-        tmem_ld32(s_addr, qa);
-        tmem_ld32(s_addr + 32, qb);
-        tmem_wait_ld();
-        reg_fence32(qa);
-        reg_fence32(qb);
-        // The columns are free again: the next S^T_h may be issued now.
-        tc_fence_before();
-        mbar_arrive(bar(L::kDqFree + h));
-        // Reduce into the fp32 accumulator with TMA bulk reduce-add, staging
-        // 32 queries x 128 values (16 KB) at a time in this half's dS^T
-        // buffer, which the completed dQ^T MMA no longer reads.  Rows at or
-        // beyond N fall outside the tensor map and are dropped by the TMA.
-        float* qstage = reinterpret_cast<float*>(smem + L::kDS + 16384 * h);
-        const bool leader = (threadIdx.x & 127) == 0;
+        {
+          uint32_t da[32], db[32];
+          tmem_ld32(dp_addr, da);
+          tmem_ld32(dp_addr + 32, db);
+          tmem_wait_ld();
+          reg_fence32(da);
+          reg_fence32(db);
+          uint32_t pd[16], pe[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (c == 1) {
-            if (leader) bulk_wait_group_read0();
-            named_bar_sync(1 + h, 128);
+          for (int v = 0; v < 16; ++v) {
+            const uint32_t* src = v < 8 ? da : db;
+            const int o = 4 * (v & 7);
+            const float4 nd = nd4[v];
+            const float2 g01 = __fadd2_rn(
+                make_float2(__uint_as_float(src[o]), __uint_as_float(src[o + 1])),
+                make_float2(nd.x, nd.y));
+            const float2 g23 = __fadd2_rn(
+                make_float2(__uint_as_float(src[o + 2]), __uint_as_float(src[o + 3])),
+                make_float2(nd.z, nd.w));
+            const float2 s01 = __fmul2_rn(make_float2(pr[4 * v], pr[4 * v + 1]), g01);
+            const float2 s23 = __fmul2_rn(make_float2(pr[4 * v + 2], pr[4 * v + 3]), g23);
+            uint32_t* dst = v < 8 ? pd : pe;
+            dst[2 * (v & 7)] = pack16x2(BF16, s01.x, s01.y);
+            dst[2 * (v & 7) + 1] = pack16x2(BF16, s23.x, s23.y);
           }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) qstage[e * 128 + r] = __uint_as_float(c == 0 ? qa[e] : qb[e]);
-          fence_proxy_async_smem();
-          named_bar_sync(1 + h, 128);
-          if (leader) {
-            tma_reduce_add_3d(&tmDQ, smem_u32(qstage), 0, i * 128 + 64 * h + 32 * c, w.bh);
-            bulk_commit_group();
-          }
+          tmem_st16(dp_addr, pd);
+          tmem_st16(dp_addr + 16, pe);
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::kDsReady));
         ++st_it;
       }
       if (!ok) break;
       // ---------------------------------------------------- dK / dV epilogue ---
-      ok = mbar_wait(bar(L::kDkvFull), unit_it & 1, wd, 34);
+      ok = mbar_wait(bar(L::kDkvFull), unit_it & 1, wd, 36);
       ok = named_bar_and(1 + h, 128, ok);
       if (!ok) break;
       ++unit_it;
@@ -439,11 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32_sync(src + 32 * c, raw);
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float a = __uint_as_float(raw[2 * e]) * mult;
-          const float b = __uint_as_float(raw[2 * e + 1]) * mult;
-          pk[e] = BF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
-        }
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack16x2(BF16, __uint_as_float(raw[2 * e]) * mult,
+                           __uint_as_float(raw[2 * e + 1]) * mult);
         if (key < p.N) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -455,7 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (warp < 8 && (threadIdx.x & 127) == 0) bulk_wait_group0();  // dQ reductions landed
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -464,13 +500,377 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ================================================================ dQ kernel ===
+
+// K_j is read by S_j and, one step later, by dQ_j; V_j only by dP_j.  Each
+// gets a ring sized to its lifetime (3 K slots, 2 V slots) so a slot's next
+// load has about two steps of MMA work to land in.
+struct DqLayout {
+  static constexpr int kQ = 0;                    // Q_i (K-major A of S = Q K^T)
+  static constexpr int kDO = kTile;               // dO_i (K-major A of dP = dO V^T)
+  static constexpr int kKSlots = 3, kVSlots = 2;
+  static constexpr int kK0 = 2 * kTile;           // K ring
+  static constexpr int kV0 = kK0 + kKSlots * kTile;  // V ring
+  static constexpr int kBar = kV0 + kVSlots * kTile;
+  enum {
+    kQFull, kQEmpty, kKFull, kKEmpty = kKFull + kKSlots, kVFull = kKEmpty + kKSlots,
+    kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots, kDpFull = kSFull + 2, kDsReady,
+    kDqFull, kDqFree, kDrain, kNumBars
+  };
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static_assert(kBytes <= 232448, "shared memory budget (227 KB) exceeded");
+};
+
+// Tensor memory: dQ [0,128)  S (two buffers) [128,256) [256,384)  dP [384,512);
+// dS (16-bit) of warpgroup h overwrites dP columns [384+64h, 384+64h+32).
+constexpr uint32_t kColDQ = 0, kColS0 = 128, kColDP2 = 384;
+
+struct DqUnit {
+  int bh, i, nsteps;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
+  DqUnit w;
+  if (CAUSAL) {
+    // Query tile i sees key tiles 0..i: descending i is longest first.
+    const int r = u / p.BH;
+    w.bh = u - r * p.BH;
+    w.i = p.n_qtiles - 1 - r;
+    w.nsteps = min(w.i + 1, p.n_kblocks);
+  } else {
+    w.bh = u / p.n_qtiles;
+    w.i = u - w.bh * p.n_qtiles;
+    w.nsteps = p.n_kblocks;
+  }
+  return w;
+}
+
+template <bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdParams p) {
+  using L = DqLayout;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0 && p.status != nullptr)
+      atomicCAS(p.status, 0u, kStatusLayout | ((blockIdx.x & 0xFFFFu) << 16));
+    return;
+  }
+  const uint32_t bar0 = sbase + L::kBar;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  Watchdog wd{p.status, abort_flag, p.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(L::kQFull), 1);
+    mbar_init(bar(L::kQEmpty), 1);
+    for (int s = 0; s < L::kKSlots; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+    }
+    for (int s = 0; s < L::kVSlots; ++s) {
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) mbar_init(bar(L::kSFull + s), 1);
+    mbar_init(bar(L::kDpFull), 1);
+    mbar_init(bar(L::kDsReady), 256);
+    mbar_init(bar(L::kDqFull), 1);
+    mbar_init(bar(L::kDqFree), 256);
+    mbar_init(bar(L::kDrain), 1);
+    mbar_fence_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  const int num_units = p.BH * p.n_qtiles;
+
+  if (warp == kWarpProducer) {
+    // -------------------------------------------------------------- producer ---
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      uint32_t k_it = 0, v_it = 0, unit_it = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = snake_unit(k, cta, G);
+        if (u >= num_units) break;
+        const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
+        ok = mbar_wait(bar(L::kQEmpty), (unit_it & 1) ^ 1, wd, 41);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::kQFull), 2 * kTile);
+        load_tile(sbase + L::kQ, &tmQ, bar(L::kQFull), w.i * 128, w.bh);
+        load_tile(sbase + L::kDO, &tmDO, bar(L::kQFull), w.i * 128, w.bh);
+        ++unit_it;
+        for (int j = 0; j < w.nsteps && ok; ++j) {
+          const uint32_t ks = k_it % L::kKSlots;
+          ok = mbar_wait(bar(L::kKEmpty + ks), ((k_it / L::kKSlots) & 1) ^ 1, wd, 42);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::kKFull + ks), kTile);
+          load_tile(sbase + L::kK0 + ks * kTile, &tmK, bar(L::kKFull + ks), j * 128, w.bh);
+          ++k_it;
+          const uint32_t vs = v_it % L::kVSlots;
+          ok = mbar_wait(bar(L::kVEmpty + vs), ((v_it / L::kVSlots) & 1) ^ 1, wd, 43);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::kVFull + vs), kTile);
+          load_tile(sbase + L::kV0 + vs * kTile, &tmV, bar(L::kVFull + vs), j * 128, w.bh);
+          ++v_it;
+        }
+      }
+      // Drain: the copies of the last ring round (and of Q) must have landed.
+      Watchdog dw = wd;
+      volatile int never = 0;
+      dw.abort_flag = &never;
+      dw.limit_ns = drain_limit_ns(wd.limit_ns);
+      if (unit_it > 0) mbar_wait(bar(L::kQFull), (unit_it - 1) & 1, dw, 44);
+      for (uint32_t it = k_it > (uint32_t)L::kKSlots ? k_it - L::kKSlots : 0u; it < k_it; ++it)
+        mbar_wait(bar(L::kKFull + it % L::kKSlots), (it / L::kKSlots) & 1, dw, 44);
+      for (uint32_t it = v_it > (uint32_t)L::kVSlots ? v_it - L::kVSlots : 0u; it < v_it; ++it)
+        mbar_wait(bar(L::kVFull + it % L::kVSlots), (it / L::kVSlots) & 1, dw, 44);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ tcgen05 issuer ---
+    // Per step j: S_j into buffer j%2 | dQ += dS_{j-1} K_{j-1} | dP_j.  The
+    // warpgroups compute P_j while dQ and dP_j run, and dS_j while S_{j+1}
+    // runs.
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);  // S, dP
+      constexpr uint32_t kIdQ = idesc_f16(128, 128, BF16, false, true);   // dQ
+      uint32_t k_it = 0, v_it = 0, unit_it = 0, step_it = 0;
+      bool ok = true;
+      const uint64_t qd = kmajor_base(sbase + L::kQ), dod = kmajor_base(sbase + L::kDO);
+      // dQ += dS K_j: A = dS from tensor memory, B = K_j read MN-major.
+      auto issue_dq = [&](uint32_t kaddr, uint32_t acc0) {
+        const uint64_t kd_mn = mnmajor_base(kaddr);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(tbase + kColDQ, tbase + kColDP2 + half_packed_col(kk),
+                     desc_plus(kd_mn, mnmajor16_off(kk)), kIdQ, kk > 0 ? 1u : acc0);
+      };
+      for (int k = 0; ok; ++k) {
+        const int u = snake_unit(k, cta, G);
+        if (u >= num_units) break;
+        const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
+        ok = mbar_wait(bar(L::kQFull), unit_it & 1, wd, 45);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t prev_kaddr = 0, prev_ks = 0;
+        for (int j = 0; j < w.nsteps && ok; ++j) {
+          const uint32_t ks = k_it % L::kKSlots;
+          ok = mbar_wait(bar(L::kKFull + ks), (k_it / L::kKSlots) & 1, wd, 46);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kaddr = sbase + L::kK0 + ks * kTile;
+          const uint32_t sb = step_it & 1;
+          // S_j = Q_i K_j^T into buffer sb (its previous S was read before
+          // the dS it produced was handed over, which the previous dQ awaited).
+          const uint64_t kd = kmajor_base(kaddr);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tbase + kColS0 + 128 * sb, desc_plus(qd, kmajor16_off(kk)),
+                       desc_plus(kd, kmajor16_off(kk)), kIdS, kk > 0);
+          mma_commit(bar(L::kSFull + sb));
+          if (j > 0) {
+            // dQ += dS_{j-1} K_{j-1}
+            ok = mbar_wait(bar(L::kDsReady), (step_it - 1) & 1, wd, 47);
+            if (!ok) break;
+            if (j == 1 && unit_it > 0) {  // the previous unit's dQ has been stored
+              ok = mbar_wait(bar(L::kDqFree), (unit_it - 1) & 1, wd, 48);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            issue_dq(prev_kaddr, j > 1 ? 1u : 0u);
+            mma_commit(bar(L::kKEmpty + prev_ks));
+          }
+          // dP_j = dO_i V_j^T (dS_{j-1} in these columns has just been consumed)
+          const uint32_t vs = v_it % L::kVSlots;
+          ok = mbar_wait(bar(L::kVFull + vs), (v_it / L::kVSlots) & 1, wd, 55);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t vd = kmajor_base(sbase + L::kV0 + vs * kTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tbase + kColDP2, desc_plus(dod, kmajor16_off(kk)),
+                       desc_plus(vd, kmajor16_off(kk)), kIdS, kk > 0);
+          mma_commit(bar(L::kDpFull));
+          mma_commit(bar(L::kVEmpty + vs));
+          if (j == w.nsteps - 1) mma_commit(bar(L::kQEmpty));  // Q_i, dO_i no longer read
+          prev_kaddr = kaddr;
+          prev_ks = ks;
+          ++k_it;
+          ++v_it;
+          ++step_it;
+        }
+        if (!ok) break;
+        // dQ += dS_last K_last, then hand dQ to the warpgroups
+        ok = mbar_wait(bar(L::kDsReady), (step_it - 1) & 1, wd, 49);
+        if (!ok) break;
+        if (w.nsteps == 1 && unit_it > 0) {
+          ok = mbar_wait(bar(L::kDqFree), (unit_it - 1) & 1, wd, 50);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        issue_dq(prev_kaddr, w.nsteps > 1 ? 1u : 0u);
+        mma_commit(bar(L::kKEmpty + prev_ks));
+        mma_commit(bar(L::kDqFull));
+        ++unit_it;
+      }
+      mma_commit(bar(L::kDrain));
+      Watchdog dw = wd;
+      volatile int never = 0;
+      dw.abort_flag = &never;
+      dw.limit_ns = drain_limit_ns(wd.limit_ns);
+      mbar_wait(bar(L::kDrain), 0, dw, 51);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ compute warpgroups ---
+    const int h = warp >> 2;                 // key half of every step
+    const int r = threadIdx.x & 127;         // TMEM lane: query row
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t dp_addr = tbase + lane_base + kColDP2 + 64 * h;
+    const uint32_t dq_addr = tbase + lane_base + kColDQ + 64 * h;
+    const float sl2 = p.scale_log2;
+    uint32_t unit_it = 0, step_it = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int u = snake_unit(k, cta, G);
+      if (u >= num_units) break;
+      const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
+      const int row = w.i * 128 + r;
+      const bool in = row < p.N;
+      const size_t grow = (size_t)w.bh * p.N + (in ? row : 0);
+      // Padding rows: LSE = +inf, D = 0, so their P and dS vanish.
+      const float nl2 = in ? -p.lse[grow] * kLog2e : -INFINITY;
+      const float nd = in ? -p.delta[grow] : 0.f;
+      const float2 sl2x2 = make_float2(sl2, sl2), nl2x2 = make_float2(nl2, nl2),
+                   nd2x2 = make_float2(nd, nd);
+      for (int j = 0; j < w.nsteps; ++j) {
+        const uint32_t sb = step_it & 1;
+        const uint32_t par = step_it & 1;
+        ok = mbar_wait(bar(L::kSFull + sb), (step_it >> 1) & 1, wd, 52);
+        ok = named_bar_and(1 + h, 128, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const bool diag = CAUSAL && (j == w.i);
+        const uint32_t s_addr = tbase + lane_base + kColS0 + 128 * sb + 64 * h;
+        // ---- P = exp2(S c - LSE log2 e), kept in fp32 for dS.  Both
+        // 32-column chunks are loaded before one wait.
+        float pr[64];
+        {
+          uint32_t sa[32], sc[32];
+          tmem_ld32(s_addr, sa);
+          tmem_ld32(s_addr + 32, sc);
+          tmem_wait_ld();
+          reg_fence32(sa);
+          reg_fence32(sc);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint32_t* src = e < 16 ? sa : sc;
+            const int o = 2 * (e & 15);
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(src[o]), __uint_as_float(src[o + 1])), sl2x2, nl2x2);
+            pr[2 * e] = ex2_approx(x.x);
+            pr[2 * e + 1] = ex2_approx(x.y);
+          }
+          if (diag) {
+#pragma unroll
+            for (int col = 0; col < 64; ++col)  // key column within the half
+              if (64 * h + col > r) pr[col] = 0.f;  // key after query
+          }
+        }
+        // ---- dS = P o (dP - D)
+        ok = mbar_wait(bar(L::kDpFull), par, wd, 53);
+        ok = named_bar_and(1 + h, 128, ok);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t da[32], db[32];
+          tmem_ld32(dp_addr, da);
+          tmem_ld32(dp_addr + 32, db);
+          tmem_wait_ld();
+          reg_fence32(da);
+          reg_fence32(db);
+          uint32_t pd[16], pe[16];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint32_t* src = e < 16 ? da : db;
+            const int o = 2 * (e & 15);
+            const float2 g = __fadd2_rn(
+                make_float2(__uint_as_float(src[o]), __uint_as_float(src[o + 1])), nd2x2);
+            const float2 sv = __fmul2_rn(make_float2(pr[2 * e], pr[2 * e + 1]), g);
+            (e < 16 ? pd : pe)[e & 15] = pack16x2(BF16, sv.x, sv.y);
+          }
+          tmem_st16(dp_addr, pd);
+          tmem_st16(dp_addr + 16, pe);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::kDsReady));
+        ++step_it;
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ dQ epilogue ---
+      ok = mbar_wait(bar(L::kDqFull), unit_it & 1, wd, 54);
+      ok = named_bar_and(1 + h, 128, ok);
+      if (!ok) break;
+      ++unit_it;
+      tc_fence_after();
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * 128 + 64 * h);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t raw[32];
+        tmem_ld32_sync(dq_addr + 32 * c, raw);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack16x2(BF16, __uint_as_float(raw[2 * e]) * p.scale,
+                           __uint_as_float(raw[2 * e + 1]) * p.scale);
+        if (in) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[4 * c + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kDqFree));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ================================================================ D kernel ===
+
 // D_i = sum_c dO_ic O_ic with one warp per row (4 values per lane, then a
-// butterfly of warp shuffles), and zero the fp32 dQ accumulator row.
+// butterfly of warp shuffles).
 template <bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                      const uint16_t* __restrict__ dout,
-                                                     float* __restrict__ delta,
-                                                     float* __restrict__ dq_acc, long rows) {
+                                                     float* __restrict__ delta, long rows) {
   const long warp0 = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -499,47 +899,30 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) delta[row] = acc;
-    reinterpret_cast<float4*>(dq_acc + row * 128)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
-// dQ = scale * dQ_acc, rounded to 16 bit; 8 values per thread and iteration.
-template <bool BF16>
-__global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ dq_acc,
-                                                      uint16_t* __restrict__ dq, float scale,
-                                                      long n8) {
-  const long t0 = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long nt = (long)gridDim.x * blockDim.x;
-  for (long t = t0; t < n8; t += nt) {
-    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
-    const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
-    uint4 r;
-    if (BF16) {
-      r = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                     pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
-    } else {
-      r = make_uint4(pack_f16x2(a.x * scale, a.y * scale), pack_f16x2(a.z * scale, a.w * scale),
-                     pack_f16x2(b.x * scale, b.y * scale), pack_f16x2(b.z * scale, b.w * scale));
-    }
-    reinterpret_cast<uint4*>(dq)[t] = r;
+template <typename Kern>
+cudaError_t launch_persistent(Kern kern, int bytes, bool* configured, const BwdLaunch& a,
+                              int units) {
+  if (!*configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    *configured = true;
   }
+  const int grid = units < a.num_sms ? units : a.num_sms;
+  kern<<<grid, kThreads, bytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, a.params);
+  return cudaGetLastError();
 }
 
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_main(const BwdLaunch& a) {
-  auto kern = bwd_main_kernel<CAUSAL, BF16>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout::kBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const int units = a.params.BH * a.params.n_kblocks;
-  const int grid = units < a.num_sms ? units : a.num_sms;
-  kern<<<grid, kThreads, BwdLayout::kBytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, a.tmDQacc,
-                                                        a.params);
-  return cudaGetLastError();
+  static bool dkv_configured = false, dq_configured = false;
+  cudaError_t e = launch_persistent(bwd_dkv_kernel<CAUSAL, BF16>, DkvLayout::kBytes,
+                                    &dkv_configured, a, a.params.BH * a.params.n_kblocks);
+  if (e != cudaSuccess) return e;
+  return launch_persistent(bwd_dq_kernel<CAUSAL, BF16>, DqLayout::kBytes, &dq_configured, a,
+                           a.params.BH * a.params.n_qtiles);
 }
 
 template <bool BF16>
@@ -550,18 +933,10 @@ cudaError_t launch_all(const BwdLaunch& a) {
   const long cap = (long)a.num_sms * 16;
   if (blocks > cap) blocks = cap;
   bwd_pre_kernel<BF16><<<(int)blocks, 256, 0, a.stream>>>(
-      static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.delta, p.dq_acc,
-      rows);
+      static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.delta, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = a.causal ? launch_main<true, BF16>(a) : launch_main<false, BF16>(a);
-  if (e != cudaSuccess) return e;
-  const long n8 = rows * 128 / 8;
-  long pblocks = (n8 + 255) / 256;
-  if (pblocks > (long)a.num_sms * 8) pblocks = (long)a.num_sms * 8;
-  bwd_post_kernel<BF16><<<(int)pblocks, 256, 0, a.stream>>>(p.dq_acc, static_cast<uint16_t*>(p.dq),
-                                                           p.scale, n8);
-  return cudaGetLastError();
+  return a.causal ? launch_main<true, BF16>(a) : launch_main<false, BF16>(a);
 }
 
 }  // namespace

@@ -18,7 +18,6 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* delta;          // workspace: D_i = sum_c dO_ic O_ic  [B*H, N]
-  float* dq_acc;         // workspace: fp32 dQ accumulator     [B*H, N, D]
   uint32_t* status;
   int BH, N;
   int n_qtiles;          // ceil(N / 128)
@@ -30,7 +29,6 @@ struct BwdParams {
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;
-  CUtensorMap tmDQacc;   // fp32 [B*H, N, 128], box 128 x 32, no swizzle (reduce-add)
   BwdParams params;
   int num_sms;
   cudaStream_t stream;

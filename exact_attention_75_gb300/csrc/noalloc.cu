@@ -1,15 +1,14 @@
 // attn_bwd_noalloc: the backward pass for callers that cannot allocate
 // device memory.
 //
-// attn_bwd needs a caller-provided workspace (the fp32 dQ accumulator and
-// the delta vector).  Some callers cannot provide one: code running inside a
+// attn_bwd needs a caller-provided workspace (the fp32 delta vector).  Some callers cannot provide one: code running inside a
 // host framework whose allocator owns all device memory and hands plugins no
 // raw allocations, real-time serving loops where a cudaMalloc (which may
 // synchronise the device) is not allowed on the request path, or embedded
 // users with a fixed memory plan.  For them this file keeps the workspace in a
 // file-scope device array of fixed size, so the call itself allocates nothing.
 //
-// The array holds kMaxRows query rows of scratch at head dim 128: it is part
+// The array holds kMaxRows query rows of scratch: it is part
 // of the library image and occupies that much memory on every GPU that loads
 // the library, until the process exits.  All calls share it.
 #include <cuda_runtime.h>
@@ -21,11 +20,10 @@
 
 namespace {
 
-constexpr size_t kMaxRows = 65536;  // B * H * N of one call
-constexpr int kHeadDim = 128;
-// Same layout attn_bwd expects: delta (fp32 per row), then dQ_acc (fp32 per
-// row and head-dim column); both parts are multiples of 256 bytes.
-constexpr size_t kScratchBytes = kMaxRows * 4 + kMaxRows * kHeadDim * 4;
+constexpr size_t kMaxRows = 4194304;  // B * H * N of one call
+constexpr int kHeadDim = 128;          // the only head dim of the backward kernels
+// The workspace attn_bwd expects: delta, fp32 per row (a multiple of 256 bytes).
+constexpr size_t kScratchBytes = kMaxRows * 4;
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 

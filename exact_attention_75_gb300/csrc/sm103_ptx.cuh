@@ -159,6 +159,12 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive at a named barrier without waiting (the waiting side uses
+// named_bar_sync with the same count).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier that also returns the OR of `pred` over the participating
 // threads (a rendezvous that carries an abort bit both ways).
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred) {

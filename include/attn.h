@@ -72,8 +72,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 
 /*
  * Bytes of device workspace attn_bwd needs: the delta vector
- * D_i = sum_c dO_ic O_ic (fp32 [B,H,N]) and the fp32 dQ accumulator
- * ([B,H,N,d]), each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ * D_i = sum_c dO_ic O_ic (fp32 [B,H,N]), rounded up to 256 bytes.  Returns 0
+ * for invalid sizes.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -88,8 +88,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *                      aligned, caller-owned; contents on entry are ignored
  *                      and on return are unspecified.
  * Only d = 128 is supported by the backward kernels (ATTN_ERR_UNSUPPORTED
- * otherwise).  dQ is accumulated in fp32 with atomic adds, so its last bits
- * may vary from run to run.
+ * otherwise).  dK, dV (per key tile) and dQ (per query tile) are each
+ * accumulated in fp32 by one CTA in a fixed order, so the results are the
+ * same from run to run.
  * Cite: FlashAttention-2 review, "Methods" (log-sum-exp kept for the backward
  * pass) and "핵심 구성요소" (backward recomputation with the log-sum-exp).
  */
@@ -107,15 +108,15 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
  * loops that must not call cudaMalloc (which can synchronise the device) on
  * the request path, or programs with a fixed memory plan.  It computes the
  * same dQ, dK, dV as attn_bwd, with the same arguments minus the workspace;
- * the scratch (delta + fp32 dQ accumulator) lives in a fixed device array
- * inside the library.
- *   Limit: B*H*N <= 65536 query rows and d = 128; larger problems return
+ * the scratch (the fp32 delta vector) lives in a fixed device array inside
+ * the library.
+ *   Limit: B*H*N <= 4194304 query rows and d = 128; larger problems return
  *   ATTN_ERR_INVALID_ARG, other head dims ATTN_ERR_UNSUPPORTED.
- *   Memory: the array (about 33.8 MB) is part of the library image and is
- *   held on every GPU that loads the library until the process exits.
- *   Sharing: all calls use the same array.  The call zeroes what must start
- *   at zero, but calls that overlap on the GPU (different streams, or
- *   different host threads, without ordering between them) race on it.
+ *   Memory: the array (16 MB) is part of the library image and is held on
+ *   every GPU that loads the library until the process exits.
+ *   Sharing: all calls use the same array: calls that overlap on the GPU
+ *   (different streams, or different host threads, without ordering between
+ *   them) race on it.
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress) with that device current; make that
  *   first call before any stream capture.

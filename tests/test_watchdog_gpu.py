@@ -54,3 +54,31 @@ def test_forward_winds_down_when_waits_run_out(attn_lib, dtype, d):
                                          to64(inp["v"][1, 2]), rows, True, w.scale)
     assert np.max(np.abs(to64(o[1, 2])[rows] - O_ref)) <= 2e-2
     assert np.max(np.abs(to64(lse[1, 2])[rows] - L_ref)) <= 5e-3
+
+
+def test_backward_winds_down_when_waits_run_out(attn_lib):
+    """The same for the backward main kernel: with a 1 us wait limit its roles
+    walk their schedules to the end without waiting, the launch reports
+    ATTN_ERR_TIMEOUT (or nothing, if no wait ran out), and a following
+    backward at the normal limit matches the oracle."""
+    import numpy as np
+    import oracle
+    from helpers import to64
+    w = wl.Workload("t", "bwd", 1, 2, 1024, 128, "bf16", True, seed=11)
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = attn_lib.fwd(q, k, v, causal=True)
+    assert attn_lib.poll_status() == (0, 0)
+    attn_lib.set_wait_limit_us(1)
+    try:
+        attn_lib.bwd(q, k, v, o, do, lse, causal=True)
+        st, detail = attn_lib.poll_status()
+    finally:
+        attn_lib.set_wait_limit_us(0)
+    assert st in (0, 4), (st, hex(detail))
+    dq, dk, dv = attn_lib.bwd(q, k, v, o, do, lse, causal=True)
+    assert attn_lib.poll_status() == (0, 0)
+    refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), True,
+                                     w.scale)
+    for g, r in zip((dq, dk, dv), refs):
+        assert np.max(np.abs(to64(g) - r)) <= 5e-2 * np.max(np.abs(r))

@@ -19,7 +19,7 @@ from helpers import to64
 
 pytestmark = pytest.mark.gpu
 REL_TOL = 5e-2
-MAX_ROWS = 65536  # B * H * N limit of the fixed scratch array
+MAX_ROWS = 4194304  # B * H * N limit of the fixed scratch array
 
 
 def _ptr(t):
