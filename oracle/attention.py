@@ -48,6 +48,7 @@ __all__ = [
     "attention_rows", "online_softmax_attention_head", "attention_backward_head",
     "attention_backward", "E4M3_MAX", "e4m3_decode", "e4m3_encode", "hadamard_matrix",
     "rotation_matrix", "quantize_blocks", "dequantize_blocks", "rmse",
+    "split_key_ranges", "attention_partial_head", "attention_split", "merge_partials",
 ]
 
 
@@ -120,6 +121,90 @@ def attention_rows(q, k, v, rows: Sequence[int], causal: bool, scale: float):
         allowed = np.arange(k.shape[0])[None, :] <= rows[:, None]
     P, lse = masked_softmax(S, allowed)
     return P @ v, lse
+
+
+# ---------------------------------------------------------------------------
+# Split over the keys, and the merge of the partial results
+# ---------------------------------------------------------------------------
+#
+# [FA3-8.3] section 7.3 (ring attention) and the "Discussion Points" of
+# [FA2-review] (a separate kernel that splits the keys for decoding) need
+# attention over a subset of the keys and a way to combine such partial
+# results; the "Insights" of [FA2-review] note that the log-sum-exp is all
+# that has to be kept besides O.  The pages give no formula; the one below is
+# the plain consequence of the softmax definition (a reading, listed in
+# the design doc): over disjoint key sets K_s with partial results
+# O_s = sum_{j in K_s} exp(S_ij - LSE_s) v_j and LSE_s = log sum_{j in K_s}
+# exp(S_ij), the result over their union is
+#   LSE = log sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+
+def split_key_ranges(n_keys: int, n_split: int, block: int = 128):
+    """Key ranges [lo, hi) of the splits the library uses: the ceil(n/block)
+    key blocks are cut into n_split contiguous runs, split s getting blocks
+    floor(s nb / n_split) .. floor((s+1) nb / n_split) (a run may be empty)."""
+    nb = -(-n_keys // block)
+    out = []
+    for s in range(n_split):
+        lo, hi = (s * nb) // n_split, ((s + 1) * nb) // n_split
+        out.append((min(lo * block, n_keys), min(hi * block, n_keys)))
+    return out
+
+
+def attention_partial_head(q, k, v, causal: bool, scale: float, key_lo: int, key_hi: int):
+    """Attention of one head over the keys [key_lo, key_hi) only: the plain
+    definition with every other key masked out (causal: key j visible to
+    query i iff j <= i, with absolute positions).  A row that sees no key of
+    the range gets LSE = -inf and O = 0.  Returns (O [N,d], LSE [N])."""
+    q = np.asarray(q, np.float64)
+    v = np.asarray(v, np.float64)
+    n = q.shape[0]
+    O = np.zeros((n, v.shape[1]), np.float64)
+    lse = np.full(n, -np.inf)
+    if key_hi <= key_lo:
+        return O, lse
+    S = scores(q, k[key_lo:key_hi], scale)
+    allowed = np.ones(S.shape, dtype=bool)
+    if causal:
+        allowed = (key_lo + np.arange(key_hi - key_lo))[None, :] <= np.arange(n)[:, None]
+    has = allowed.any(axis=1)
+    if has.any():
+        P, l = masked_softmax(S[has], allowed[has])
+        O[has] = P @ v[key_lo:key_hi]
+        lse[has] = l
+    return O, lse
+
+
+def attention_split(q, k, v, causal: bool, scale: float, n_split: int, block: int = 128):
+    """Partial results of every split, batched.  q,k,v: [B,H,N,d] ->
+    O_parts [n_split,B,H,N,d], LSE_parts [n_split,B,H,N]."""
+    q = np.asarray(q, np.float64)
+    B, H, N, d = q.shape
+    ranges = split_key_ranges(N, n_split, block)
+    O = np.zeros((n_split, B, H, N, np.shape(v)[-1]), np.float64)
+    L = np.full((n_split, B, H, N), -np.inf)
+    for s, (lo, hi) in enumerate(ranges):
+        for b in range(B):
+            for h in range(H):
+                O[s, b, h], L[s, b, h] = attention_partial_head(q[b, h], k[b, h], v[b, h],
+                                                                causal, scale, lo, hi)
+    return O, L
+
+
+def merge_partials(O_parts, LSE_parts):
+    """Combine partial results over disjoint key sets (axis 0 = split):
+    LSE = log sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  Rows where
+    every LSE_s is -inf get LSE = -inf and O = 0."""
+    O_parts = np.asarray(O_parts, np.float64)
+    L = np.asarray(LSE_parts, np.float64)
+    mx = np.max(L, axis=0)
+    finite = np.isfinite(mx)
+    safe = np.where(finite, mx, 0.0)
+    w = np.where(np.isfinite(L), np.exp(L - safe[None]), 0.0)
+    tot = w.sum(axis=0)
+    lse = np.where(finite, safe + np.log(np.where(finite, tot, 1.0)), -np.inf)
+    scale = np.where(finite, 1.0 / np.where(finite, tot, 1.0), 0.0)
+    O = np.einsum("s...,s...d->...d", w * scale[None], O_parts)
+    return O, lse
 
 
 # ---------------------------------------------------------------------------

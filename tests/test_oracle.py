@@ -363,3 +363,83 @@ def test_fp8_recipe_error_floor():
         O_q, _ = oracle.attention(dq(q, s), dq(k, s), dq(v), True, w.scale)
         res[outl] = oracle.rmse(O_q, O_ref)
     assert res[False] < 0.01 and res[True] > 0.03, res
+
+
+# ---------------------------------------------------------------------------
+# Split over the keys + merge (the single-GPU form of ring attention's
+# exchange, [FA3-8.3] section 7.3; decoding split, [FA2-review] "Discussion
+# Points").  Pins: the merge of partial results over a partition of the keys
+# is, by the softmax definition, exactly the attention over all keys.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,block,n_split", [(300, 32, 2), (300, 32, 5), (257, 64, 3),
+                                              (96, 32, 7), (128, 128, 1), (40, 16, 40)])
+def test_split_then_merge_is_full_attention(causal, N, block, n_split):
+    rng = np.random.default_rng(N + n_split)
+    q, k, v = (rng.standard_normal((1, 2, N, 16)) for _ in range(3))
+    Op, Lp = oracle.attention_split(q, k, v, causal, 0.3, n_split, block=block)
+    O, L = oracle.merge_partials(Op, Lp)
+    Or, Lr = oracle.attention(q, k, v, causal, 0.3)
+    assert np.max(np.abs(O - Or)) < 1e-12 and np.max(np.abs(L - Lr)) < 1e-12
+
+
+def test_split_merge_large_logits_stays_finite():
+    # logits of order 1e3: a merge that exponentiates LSE_s without the
+    # running maximum would overflow
+    rng = np.random.default_rng(5)
+    q, k, v = (rng.standard_normal((1, 1, 200, 8)) for _ in range(3))
+    Op, Lp = oracle.attention_split(q, k, v, True, 400.0, 4, block=32)
+    O, L = oracle.merge_partials(Op, Lp)
+    Or, Lr = oracle.attention(q, k, v, True, 400.0)
+    assert np.isfinite(O).all() and np.max(np.abs(O - Or)) < 1e-9
+    assert np.max(np.abs(L - Lr) / np.abs(Lr)) < 1e-12
+
+
+def test_partial_lse_brute_force():
+    rng = np.random.default_rng(9)
+    q, k, v = (rng.standard_normal((9, 3)) for _ in range(3))
+    O, L = oracle.attention_partial_head(q, k, v, True, 0.7, 3, 7)
+    for i in range(9):
+        keys = [j for j in range(3, 7) if j <= i]
+        if not keys:
+            assert L[i] == -np.inf and not O[i].any()
+            continue
+        e = [math.exp(0.7 * sum(q[i, c] * k[j, c] for c in range(3))) for j in keys]
+        assert abs(L[i] - math.log(sum(e))) < 1e-13
+        want = [sum(e[t] * v[j, c] for t, j in enumerate(keys)) / sum(e) for c in range(3)]
+        assert np.max(np.abs(O[i] - want)) < 1e-13
+
+
+def test_merge_order_free_and_associative():
+    rng = np.random.default_rng(11)
+    Op = rng.standard_normal((3, 5, 4))
+    Lp = rng.standard_normal((3, 5)) * 3
+    O, L = oracle.merge_partials(Op, Lp)
+    Or, Lr = oracle.merge_partials(Op[::-1], Lp[::-1])
+    O01, L01 = oracle.merge_partials(Op[:2], Lp[:2])
+    Oa, La = oracle.merge_partials(np.stack([O01, Op[2]]), np.stack([L01, Lp[2]]))
+    for a, b in ((O, Or), (L, Lr), (O, Oa), (L, La)):
+        assert np.max(np.abs(a - b)) < 1e-13
+
+
+def test_empty_split_is_neutral_and_all_empty_rows():
+    rng = np.random.default_rng(13)
+    Op = rng.standard_normal((2, 3, 4))
+    Lp = rng.standard_normal((2, 3))
+    O, L = oracle.merge_partials(Op, Lp)
+    Oe, Le = oracle.merge_partials(np.concatenate([Op, np.full((1, 3, 4), 7.0)]),
+                                   np.concatenate([Lp, np.full((1, 3), -np.inf)]))
+    assert np.max(np.abs(O - Oe)) < 1e-15 and np.max(np.abs(L - Le)) < 1e-15
+    Oz, Lz = oracle.merge_partials(np.ones((2, 3, 4)), np.full((2, 3), -np.inf))
+    assert not Oz.any() and (Lz == -np.inf).all()
+
+
+@pytest.mark.parametrize("n,ns", [(8192, 4), (300, 5), (100, 3), (129, 2)])
+def test_split_key_ranges_tile_the_keys(n, ns):
+    r = oracle.split_key_ranges(n, ns)
+    assert r[0][0] == 0 and r[-1][1] == n and len(r) == ns
+    for (a, b), (c, _) in zip(r, r[1:]):
+        assert b == c and a <= b
+    for a, _ in r:
+        assert a % 128 == 0 or a == n
