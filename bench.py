@@ -253,6 +253,45 @@ def available_components(attn, step_probe=None):
                                                            ",".join(COMPONENTS)).split(",")]
 
 
+SPLIT_KV_N = 4  # key splits of the split-KV measurement
+
+
+def split_kv_timing(attn, st, w, stream, n_split, iters=20):
+    """The split over the keys + merge on the same workload, timed apart from
+    the step: attn_fwd_split (n_split runs of key blocks) and attn_merge,
+    each with CUDA events on the launching stream after 3 warm-up calls."""
+    BH, N, d = w.B * w.H, w.N, w.d
+    o_part = torch.empty((n_split, w.B, w.H, N, d), dtype=st.q.dtype, device=st.q.device)
+    l_part = torch.empty((n_split, w.B, w.H, N), dtype=torch.float32, device=st.q.device)
+    o = torch.empty_like(st.q)
+    lse = torch.empty((w.B, w.H, N), dtype=torch.float32, device=st.q.device)
+    for _ in range(3):
+        attn.fwd_split(st.q, st.k, st.v, n_split, causal=w.causal, out=o_part, lse=l_part)
+        attn.merge(o_part, l_part, out=o, lse=lse)
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ts, tm = [], []
+    for _ in range(iters):
+        e[0].record(stream)
+        attn.fwd_split(st.q, st.k, st.v, n_split, causal=w.causal, out=o_part, lse=l_part)
+        e[1].record(stream)
+        attn.merge(o_part, l_part, out=o, lse=lse)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        ts.append(e[0].elapsed_time(e[1]))
+        tm.append(e[1].elapsed_time(e[2]))
+    status = attn.poll_status()
+    if status[0] != 0:
+        raise RuntimeError(f"device status after the split-KV timing: {status}")
+    ms_s, ms_m = statistics.mean(ts), statistics.mean(tm)
+    # algorithmic bytes of the merge: read the partial O and LSE, write O, LSE
+    merge_bytes = n_split * (BH * N * d * 2 + BH * N * 4) + BH * N * d * 2 + BH * N * 4
+    return {"n_split": n_split, "fwd_split_ms": round(ms_s, 4), "merge_ms": round(ms_m, 4),
+            "tflops": round(w.fwd_flops() / ((ms_s + ms_m) * 1e-3) / 1e12, 1),
+            "merge_gbs": round(merge_bytes / (ms_m * 1e-3) / 1e9, 1),
+            "merge_bytes": merge_bytes}
+
+
 def run_gpu(args, rank, world, local_rank):
     import exact_attention_75_gb300 as attn
     dev = torch.device("cuda", local_rank)
@@ -334,11 +373,13 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
+    split = split_kv_timing(attn, st, w, stream, n_split=SPLIT_KV_N)
+
     step_flops = sum(flops[c] for c in comps)
     ms_step = ms_total / args.steps
     if world > 1:
         ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
-    return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks,
+    return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks, split=split,
                 flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
                 launches=sum(LAUNCHES[c] for c in comps) * args.steps)
 
@@ -460,6 +501,16 @@ def main():
             "gpu_launches": r["launches"],
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}}
+    if r.get("split"):
+        sp = dict(r["split"])
+        mb = sp.pop("merge_bytes")
+        sp["note"] = ("split over the keys + merge, timed apart from the step (not in value); "
+                      "tflops = forward FLOPs / (split forward + merge)")
+        sp["merge_roofline"] = {"bound": "hbm", "achieved": sp["merge_gbs"],
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": round(sp["merge_gbs"] / peaks["hbm_gbs"], 4),
+                                "algorithmic_bytes": mb}
+        line["split_kv"] = sp
     if not args.no_cpu_baseline:
         tf, dt, heads, cores = cpu_oracle_sample()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores,

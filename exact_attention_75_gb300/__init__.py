@@ -19,9 +19,9 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["AttnError", "lib", "lib_path", "fwd", "bwd", "bwd_workspace_bytes", "quantize_fp8",
-           "fwd_fp8", "poll_status", "set_wait_limit_us", "selftest_wait_timeout", "num_sms",
-           "STATUS"]
+__all__ = ["AttnError", "lib", "lib_path", "fwd", "fwd_split", "merge", "bwd",
+           "bwd_workspace_bytes", "quantize_fp8", "fwd_fp8", "poll_status", "set_wait_limit_us",
+           "selftest_wait_timeout", "num_sms", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
     u32p = ctypes.POINTER(ctypes.c_uint32)
     sigs = {
         "attn_fwd": ([vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp], i),
+        "attn_fwd_split": ([vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp], i),
+        "attn_merge": ([vp, vp, i, vp, vp, i, i, i, i, i, vp], i),
         "attn_bwd_workspace_bytes": ([i, i, i, i], sz),
         "attn_bwd": ([vp] * 10 + [sz, i, i, i, i, i, f, i, vp], i),
         "attn_quantize_fp8": ([vp, vp, vp, i, i, i, i, i, vp, i, vp], i),
@@ -125,6 +127,53 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
                             int(bool(causal)), float(scale), _dtype_code(q), _stream(q))
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def fwd_split(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_split: int,
+              causal: bool = False, scale: Optional[float] = None,
+              out: Optional[torch.Tensor] = None,
+              lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Partial results of attention over n_split runs of whole 128-key blocks:
+    O_parts [n_split,B,H,N,d] (q's dtype), LSE_parts [n_split,B,H,N] fp32
+    (-inf where a row sees no key of the split)."""
+    B, H, N, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((n_split, B, H, N, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((n_split, B, H, N), dtype=torch.float32, device=q.device)
+    if tuple(out.shape) != (n_split, B, H, N, d) or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [n_split, B, H, N, d] tensor of q's dtype")
+    if tuple(lse.shape) != (n_split, B, H, N) or lse.dtype != torch.float32:
+        raise ValueError("lse must be a float32 [n_split, B, H, N] tensor")
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(n_split),
+                                  B, H, N, d, int(bool(causal)), float(scale), _dtype_code(q),
+                                  _stream(q))
+    _check(st, "attn_fwd_split")
+    return out, lse
+
+
+def merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: Optional[torch.Tensor] = None,
+          lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Combine partial results over disjoint key sets: LSE = log sum exp(LSE_s),
+    O = sum_s exp(LSE_s - LSE) O_s.  o_parts [S,B,H,N,d], lse_parts [S,B,H,N]."""
+    if o_parts.dim() != 5 or not o_parts.is_cuda or not o_parts.is_contiguous():
+        raise ValueError("o_parts must be a contiguous CUDA [n_split, B, H, N, d] tensor")
+    S, B, H, N, d = o_parts.shape
+    if tuple(lse_parts.shape) != (S, B, H, N) or lse_parts.dtype != torch.float32 \
+            or not lse_parts.is_contiguous():
+        raise ValueError("lse_parts must be a contiguous float32 [n_split, B, H, N] tensor")
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=o_parts.dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        st = lib().attn_merge(_ptr(o_parts), _ptr(lse_parts), int(S), _ptr(out), _ptr(lse),
+                              B, H, N, d, _dtype_code(o_parts), _stream(o_parts))
+    _check(st, "attn_merge")
     return out, lse
 
 

@@ -14,6 +14,7 @@
 #include "bwd.cuh"
 #include "fp8.cuh"
 #include "fwd.cuh"
+#include "merge.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -132,6 +133,46 @@ attn_status fill_fwd_common(FwdLaunch* a, DeviceInfo* di, int B, int H, int N, f
 
 using namespace attn;
 
+namespace {
+
+// attn_fwd with the keys cut into n_split runs of whole 128-key blocks, each
+// split writing its partial O / LSE at its own offset.
+attn_status fwd_split_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int n_split, int B, int H, int N, int d, int causal, float scale,
+                           attn_dtype dtype, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  if (n_split < 1 || n_split > 256) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  attn_status st = device_info(&di);
+  if (st != ATTN_OK) return st;
+  FwdLaunch a;
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int64_t BH = (int64_t)B * H;
+  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmK, k, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, BH, 64, 128))
+    return ATTN_ERR_CUDA;
+  fill_fwd_common(&a, di, B, H, N, scale, stream, o, lse);
+  FwdParams& p = a.params;
+  if ((int64_t)p.num_units * n_split > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
+  p.n_split = n_split;
+  p.num_units *= n_split;
+  p.o_split = (size_t)BH * N * d;
+  p.lse_split = (size_t)BH * N;
+  cudaError_t e = launch_fwd(a, d, causal != 0, dtype == ATTN_BF16);
+  return launch_result(e);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* attn_status_string(attn_status s) {
@@ -157,31 +198,44 @@ attn_status attn_set_wait_limit_us(uint64_t limit_us) {
   return ATTN_OK;
 }
 
+
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int N, int d, int causal, float scale, attn_dtype dtype,
                      void* stream) {
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  return fwd_split_impl(q, k, v, o, lse, 1, B, H, N, d, causal, scale, dtype, stream);
+}
+
+attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_part,
+                           float* lse_part, int n_split, int B, int H, int N, int d, int causal,
+                           float scale, attn_dtype dtype, void* stream) {
+  return fwd_split_impl(q, k, v, o_part, lse_part, n_split, B, H, N, d, causal, scale, dtype,
+                        stream);
+}
+
+attn_status attn_merge(const void* o_part, const float* lse_part, int n_split, void* o,
+                       float* lse, int B, int H, int N, int d, attn_dtype dtype, void* stream) {
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (n_split < 1 || n_split > 256) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
   if (st != ATTN_OK) return st;
-  FwdLaunch a;
-  const CUtensorMapDataType dt =
-      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const int64_t BH = (int64_t)B * H;
-  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmK, k, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmV, v, dt, 2, d, N, BH, 64, 128))
-    return ATTN_ERR_CUDA;
-  fill_fwd_common(&a, di, B, H, N, scale, stream, o, lse);
-  cudaError_t e = launch_fwd(a, d, causal != 0, dtype == ATTN_BF16);
-  return launch_result(e);
+  MergeLaunch a;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.o = o;
+  a.lse = lse;
+  a.rows = (long)B * H * N;
+  a.n_split = n_split;
+  a.d = d;
+  a.bf16 = dtype == ATTN_BF16;
+  a.num_sms = di->num_sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(launch_merge(a));
 }
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {

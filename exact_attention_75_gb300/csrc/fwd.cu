@@ -74,12 +74,18 @@ struct FwdLayout {
 
 struct Unit {
   int bh, qp;
-  int nb[2];  // K/V blocks visited by query tile 0 / 1 (0 = tile absent)
+  int split;  // key split of this unit (0 without a split)
+  int kb0;    // first key block of the split
+  int nb[2];  // K/V blocks visited by query tile 0 / 1 (0: tile absent or no key in the split)
 };
 
 template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   Unit w;
+  w.split = u % p.n_split;  // splits of one query-tile pair are neighbours
+  u /= p.n_split;
+  w.kb0 = (w.split * p.n_kblocks) / p.n_split;
+  const int kb1 = ((w.split + 1) * p.n_kblocks) / p.n_split;
   if (CAUSAL) {
     // Longest first: the heaviest query-tile pairs of every head come first.
     const int r = u / p.BH;
@@ -95,7 +101,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     if (tile >= p.n_qtiles) {
       w.nb[t] = 0;
     } else {
-      w.nb[t] = CAUSAL ? min(tile + 1, p.n_kblocks) : p.n_kblocks;
+      const int visible = CAUSAL ? min(tile + 1, p.n_kblocks) : p.n_kblocks;
+      w.nb[t] = max(0, min(visible, kb1) - w.kb0);
     }
   }
   return w;
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = snake_unit(k, cta, G);
         if (u >= p.num_units) break;
         const Unit w = decode_unit<CAUSAL>(u, p);
+        if (max(w.nb[0], w.nb[1]) == 0) continue;  // no key of the split is visible
         for (int t = 0; t < 2 && ok; ++t) {
           if (w.nb[t] == 0) continue;
           ok = mbar_wait(bar(L::kQEmpty + t), (q_it[t] & 1) ^ 1, wd, 1);
@@ -187,14 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (FP8) {
               // K: [128 keys][128 d] bytes; V^T: [128 d][128 keys] bytes.
               if (which == 0)
-                tma_load_3d(dst, &tmK, bar(L::kKvFull + slot), 0, j * 128, w.bh);
+                tma_load_3d(dst, &tmK, bar(L::kKvFull + slot), 0, (w.kb0 + j) * 128, w.bh);
               else
-                tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), j * 128, 0, w.bh);
+                tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), (w.kb0 + j) * 128, 0, w.bh);
             } else {
 #pragma unroll
               for (int h = 0; h < D / 64; ++h)
                 tma_load_3d(dst + h * 16384, which ? &tmV : &tmK, bar(L::kKvFull + slot),
-                            h * 64, j * 128, w.bh);
+                            h * 64, (w.kb0 + j) * 128, w.bh);
             }
             ++kv_it;
           }
@@ -236,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= p.num_units) break;
       const Unit w = decode_unit<CAUSAL>(u, p);
       const int nbmax = max(w.nb[0], w.nb[1]);
+      if (nbmax == 0) continue;  // the same skip in every role
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (w.nb[t] == 0) continue;
@@ -307,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = decode_unit<CAUSAL>(u, p);
       const int nb0 = w.nb[0], nb1 = w.nb[1];
       const int nbmax = max(nb0, nb1);
+      if (nbmax == 0) continue;  // the same skip in every role
       // Q tiles and K_0 are in shared memory: S_t(0) = Q_t K_0^T.
       aborted = named_bar_or(kBarKv, 64, aborted);
       uint32_t kslot = kv_it % L::kSlots;
@@ -398,9 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= p.num_units) break;
       const Unit w = decode_unit<CAUSAL>(u, p);
       const int nb = w.nb[t];
-      if (nb == 0) continue;
       const int tile = 2 * w.qp + t;
       const int row = tile * 128 + r;
+      // this split's partial O and LSE
+      uint16_t* const obase = static_cast<uint16_t*>(p.o) + w.split * p.o_split;
+      float* const lbase = p.lse + w.split * p.lse_split;
+      if (nb == 0) {
+        // A query tile that sees no key of this split: O = 0, LSE = -inf.
+        if (tile < p.n_qtiles && row < p.N) {
+          const size_t grow = (size_t)w.bh * p.N + row;
+          uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+          lbase[grow] = -INFINITY;
+        }
+        continue;
+      }
       float m = -INFINITY;  // running max of the log2-scaled scores (reference value)
       float l = 0.f;        // running sum of exp2(x - m)
       // E4M3 path: this row's Q block scale and the head's largest V scale
@@ -436,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s[128];
         float g0 = 1.f, g1 = 1.f;
         if constexpr (FP8) {
-          // keys [0,64) and [64,128) of block j have their own K and V scales
-          const int b0 = 2 * j, b1 = min(2 * j + 1, p.n_sblocks - 1);
+          // keys [0,64) and [64,128) of the block have their own K and V scales
+          const int b0 = 2 * (w.kb0 + j), b1 = min(b0 + 1, p.n_sblocks - 1);
           const float f0 = fq * ksc[b0];
           const float f1 = fq * ksc[b1];
           g0 = vsc[b0] / sv_max;
@@ -459,10 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
         }
-        const bool diag = CAUSAL && (j == tile);
-        const bool tail = (j == p.n_kblocks - 1) && (p.N & 127);
+        const int jk = w.kb0 + j;  // key block index
+        const bool diag = CAUSAL && (jk == tile);
+        const bool tail = (jk == p.n_kblocks - 1) && (p.N & 127);
         if (diag || tail) {
-          const int kbase = j * 128;
+          const int kbase = jk * 128;
           const int lim = CAUSAL ? min(row, p.N - 1) : (p.N - 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
@@ -557,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = (FP8 ? sv_max : 1.0f) / l;
       const size_t grow = (size_t)w.bh * p.N + row;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
+      uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t raw[32];
@@ -575,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             orow[c * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (row < p.N) p.lse[grow] = (m + log2f(l)) * 0.69314718055994530942f;
+      if (row < p.N) lbase[grow] = (m + log2f(l)) * 0.69314718055994530942f;
       tc_fence_before();
     }
   }

@@ -15,7 +15,12 @@ struct FwdParams {
   int n_qtiles;         // ceil(N / 128)
   int n_pairs;          // ceil(n_qtiles / 2): work units per head
   int n_kblocks;        // ceil(N / 128)
-  int num_units;        // BH * n_pairs
+  int num_units;        // n_split * BH * n_pairs
+  // Split over the keys: split s covers key blocks [s nb / n_split,
+  // (s+1) nb / n_split) and writes its partial O / LSE at o + s * o_split,
+  // lse + s * lse_split (elements).  n_split = 1: the whole key range.
+  int n_split = 1;
+  size_t o_split = 0, lse_split = 0;
   float scale_log2;     // scale * log2(e)
   unsigned long long wait_limit_ns;
   // E4M3 path only: per-(head, 64-row block) fp32 scales of Q, K and V.

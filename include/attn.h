@@ -71,6 +71,42 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      void* stream);
 
 /*
+ * Forward pass over a split of the keys: the ceil(N/128) key blocks are cut
+ * into n_split contiguous runs (split s = blocks [s nb / n_split,
+ * (s+1) nb / n_split), a run may be empty), and split s writes the partial
+ * result of its keys alone:
+ *   o_part   : [n_split, B, H, N, d] same dtype as q; partial O_s (each row
+ *              normalised over the split's visible keys), written.
+ *   lse_part : [n_split, B, H, N] fp32; LSE_s = log sum over the split's
+ *              visible keys of exp(scale q.k); -inf (and O_s = 0) for a row
+ *              that sees no key of the split.  Written.
+ * Other arguments as in attn_fwd; 1 <= n_split <= 256.  With n_split = 1 the
+ * output equals attn_fwd's.  attn_merge combines the partial results.
+ * Cite: "8.3 FlashAttention-3" section 7.3 (ring attention: attention
+ * computed over parts of the keys) and the FlashAttention-2 review,
+ * "Discussion Points" (a decoding kernel that splits the keys).
+ */
+attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_part,
+                           float* lse_part, int n_split, int B, int H, int N, int d, int causal,
+                           float scale, attn_dtype dtype, void* stream);
+
+/*
+ * Merge partial results over disjoint key sets (as written by
+ * attn_fwd_split): per row, LSE = log sum_s exp(LSE_s) and
+ * O = sum_s exp(LSE_s - LSE) O_s, computed in fp32 with the running maximum;
+ * rows where every LSE_s is -inf get O = 0, LSE = -inf.
+ *   o_part   : [n_split, B, H, N, d] fp16/bf16 (dtype), read only.
+ *   lse_part : [n_split, B, H, N] fp32, read only.
+ *   o        : [B, H, N, d] dtype, written;  lse : [B, H, N] fp32, written.
+ * d in {64, 128}; 1 <= n_split <= 256.
+ * Cite: the FlashAttention-2 review, "Insights" (the log-sum-exp is all that
+ * has to be kept besides O); the combine formula follows from the softmax
+ * definition over the union of the key sets.
+ */
+attn_status attn_merge(const void* o_part, const float* lse_part, int n_split, void* o,
+                       float* lse, int B, int H, int N, int d, attn_dtype dtype, void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs: the delta vector
  * D_i = sum_c dO_ic O_ic (fp32 [B,H,N]), rounded up to 256 bytes.  Returns 0
  * for invalid sizes.
