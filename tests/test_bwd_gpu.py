@@ -107,3 +107,18 @@ def test_bwd_argument_errors(attn_lib):
     assert L.attn_bwd(*args(128, need - 1)) == 1       # workspace too small
     assert L.attn_bwd(*args(128, need)) == 0
     assert attn_lib.poll_status()[0] == 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_is_deterministic(attn_lib, causal):
+    """dK, dV (per key tile) and dQ (per query tile) are each accumulated by
+    one CTA in a fixed order, with no atomics: two runs give the same bits."""
+    w = wl.Workload("det", "bwd", 2, 4, 2000, 128, "bf16", causal, seed=21)
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = attn_lib.fwd(q, k, v, causal=causal)
+    g1 = attn_lib.bwd(q, k, v, o, do, lse, causal=causal)
+    g2 = attn_lib.bwd(q, k, v, o, do, lse, causal=causal)
+    assert attn_lib.poll_status() == (0, 0)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
