@@ -49,6 +49,7 @@ __all__ = [
     "attention_backward", "E4M3_MAX", "e4m3_decode", "e4m3_encode", "hadamard_matrix",
     "rotation_matrix", "quantize_blocks", "dequantize_blocks", "rmse",
     "split_key_ranges", "attention_partial_head", "attention_split", "merge_partials",
+    "kv_head_of", "attention_gqa", "attention_backward_gqa",
 ]
 
 
@@ -205,6 +206,58 @@ def merge_partials(O_parts, LSE_parts):
     scale = np.where(finite, 1.0 / np.where(finite, tot, 1.0), 0.0)
     O = np.einsum("s...,s...d->...d", w * scale[None], O_parts)
     return O, lse
+
+
+# ---------------------------------------------------------------------------
+# Grouped query heads (GQA / MQA)
+# ---------------------------------------------------------------------------
+#
+# The "Insights" of [FA2-review] link GQA ("Training Generalized Multi-Query
+# Transformer Models") without spelling it out.  Reading (listed in
+# the design doc): with Hq query heads and Hkv key/value heads, Hkv dividing Hq and
+# G = Hq / Hkv, query head h attends with key/value head h // G (contiguous
+# groups; Hkv = 1 is multi-query attention).  Each query head's attention is
+# the plain definition; the gradient of a shared key/value head is the sum of
+# the gradients it receives from the query heads of its group.
+
+def kv_head_of(h: int, Hq: int, Hkv: int) -> int:
+    """Key/value head used by query head h."""
+    return h // (Hq // Hkv)
+
+
+def attention_gqa(q, k, v, causal: bool, scale: float):
+    """q: [B,Hq,N,d], k, v: [B,Hkv,N,d] -> O [B,Hq,N,d], LSE [B,Hq,N]."""
+    q = np.asarray(q, np.float64)
+    B, Hq, N, d = q.shape
+    Hkv = np.shape(k)[1]
+    assert Hq % Hkv == 0
+    O = np.empty((B, Hq, N, np.shape(v)[-1]), np.float64)
+    L = np.empty((B, Hq, N), np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            O[b, h], L[b, h], _ = attention_head(q[b, h], k[b, g], v[b, g], causal, scale)
+    return O, L
+
+
+def attention_backward_gqa(q, k, v, do, causal: bool, scale: float):
+    """dQ [B,Hq,N,d], dK / dV [B,Hkv,N,d]: per query head the plain backward,
+    dK and dV summed over the query heads of each group."""
+    q = np.asarray(q, np.float64)
+    B, Hq, N, d = q.shape
+    Hkv = np.shape(k)[1]
+    dQ = np.empty(q.shape, np.float64)
+    dK = np.zeros((B, Hkv) + np.shape(k)[2:], np.float64)
+    dV = np.zeros((B, Hkv) + np.shape(v)[2:], np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            dq, dk, dv, _ = attention_backward_head(q[b, h], k[b, g], v[b, g], do[b, h], causal,
+                                                    scale)
+            dQ[b, h] = dq
+            dK[b, g] += dk
+            dV[b, g] += dv
+    return dQ, dK, dV
 
 
 # ---------------------------------------------------------------------------

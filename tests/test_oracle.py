@@ -443,3 +443,57 @@ def test_split_key_ranges_tile_the_keys(n, ns):
         assert b == c and a <= b
     for a, _ in r:
         assert a % 128 == 0 or a == n
+
+
+# ---------------------------------------------------------------------------
+# Grouped query heads (GQA / MQA; linked from the "Insights" of [FA2-review]).
+# Pins: identity with plain attention on K/V repeated over each group, the
+# sum-over-group rule for dK/dV by finite differences, Hkv = Hq.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (6, 1), (8, 4), (3, 3)])
+def test_gqa_equals_attention_on_repeated_kv(causal, Hq, Hkv):
+    rng = np.random.default_rng(Hq * 10 + Hkv)
+    q = rng.standard_normal((2, Hq, 33, 8))
+    k, v = (rng.standard_normal((2, Hkv, 33, 8)) for _ in range(2))
+    do = rng.standard_normal(q.shape)
+    G = Hq // Hkv
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    O, L = oracle.attention_gqa(q, k, v, causal, 0.4)
+    Or, Lr = oracle.attention(q, kr, vr, causal, 0.4)
+    assert np.max(np.abs(O - Or)) == 0.0 and np.max(np.abs(L - Lr)) == 0.0
+    dQ, dK, dV = oracle.attention_backward_gqa(q, k, v, do, causal, 0.4)
+    dQr, dKr, dVr = oracle.attention_backward(q, kr, vr, do, causal, 0.4)
+    assert np.max(np.abs(dQ - dQr)) < 1e-14
+    assert np.max(np.abs(dK - dKr.reshape(2, Hkv, G, 33, 8).sum(axis=2))) < 1e-13
+    assert np.max(np.abs(dV - dVr.reshape(2, Hkv, G, 33, 8).sum(axis=2))) < 1e-13
+
+
+def test_gqa_shared_kv_gradient_by_finite_differences():
+    rng = np.random.default_rng(17)
+    q = rng.standard_normal((1, 4, 7, 3))
+    k, v = (rng.standard_normal((1, 2, 7, 3)) for _ in range(2))
+    do = rng.standard_normal(q.shape)
+    _, dK, dV = oracle.attention_backward_gqa(q, k, v, do, True, 0.6)
+
+    def loss(kk, vv):
+        O, _ = oracle.attention_gqa(q, kk, vv, True, 0.6)
+        return float(np.sum(O * do))
+
+    eps = 1e-6
+    for (g, i, c) in [(0, 3, 1), (1, 6, 2), (1, 0, 0)]:
+        kp, km = k.copy(), k.copy()
+        kp[0, g, i, c] += eps
+        km[0, g, i, c] -= eps
+        assert abs((loss(kp, v) - loss(km, v)) / (2 * eps) - dK[0, g, i, c]) < 1e-7
+        vp, vm = v.copy(), v.copy()
+        vp[0, g, i, c] += eps
+        vm[0, g, i, c] -= eps
+        assert abs((loss(k, vp) - loss(k, vm)) / (2 * eps) - dV[0, g, i, c]) < 1e-7
+
+
+def test_kv_head_mapping_is_contiguous_groups():
+    assert [oracle.kv_head_of(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    assert [oracle.kv_head_of(h, 4, 1) for h in range(4)] == [0, 0, 0, 0]
+    assert [oracle.kv_head_of(h, 4, 4) for h in range(4)] == [0, 1, 2, 3]
