@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
     sigs = {
         "attn_fwd": ([vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp], i),
         "attn_fwd_split": ([vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp], i),
+        "attn_fwd_gqa": ([vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp], i),
+        "attn_bwd_gqa": ([vp] * 10 + [sz, i, i, i, i, i, i, f, i, vp], i),
         "attn_merge": ([vp, vp, i, vp, vp, i, i, i, i, i, vp], i),
         "attn_bwd_workspace_bytes": ([i, i, i, i], sz),
         "attn_bwd": ([vp] * 10 + [sz, i, i, i, i, i, f, i, vp], i),
@@ -111,10 +113,27 @@ def _check_qkv(*ts: torch.Tensor) -> Tuple[int, int, int, int]:
     return B, H, N, d
 
 
+def _check_kv_heads(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
+    """Key/value heads of k, v for query tensor q (GQA when fewer than q's)."""
+    if k.dim() != 4 or k.shape != v.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must share shape and q's dtype")
+    if k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:]:
+        raise ValueError("k, v must be [B, Hkv, N, d] with q's B, N, d")
+    if q.shape[1] % k.shape[1] != 0:
+        raise ValueError("the number of key/value heads must divide the query heads")
+    for t in (k, v):
+        if not t.is_cuda or t.device != q.device or not t.is_contiguous():
+            raise ValueError("k, v must be contiguous tensors on q's device")
+    return int(k.shape[1])
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
         lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O, LSE = attention(q, k, v).  q,k,v: [B,H,N,d] fp16/bf16, d in {64,128}."""
+    """O, LSE = attention(q, k, v).  q: [B,H,N,d], k, v: [B,Hkv,N,d] (Hkv
+    divides H; fewer heads = grouped query heads) fp16/bf16, d in {64,128}."""
+    if k.dim() == 4 and q.dim() == 4 and k.shape[1] != q.shape[1]:
+        return _fwd_gqa(q, k, v, causal, scale, out, lse)
     B, H, N, d = _check_qkv(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -177,14 +196,32 @@ def merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: Optional[torch.Te
     return out, lse
 
 
+def _fwd_gqa(q, k, v, causal, scale, out, lse):
+    B, H, N, d = _check_qkv(q)
+    Hkv = _check_kv_heads(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_qkv(q, out)
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                                int(bool(causal)), float(scale), _dtype_code(q), _stream(q))
+    _check(st, "attn_fwd_gqa")
+    return out, lse
+
+
 def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(lib().attn_bwd_workspace_bytes(B, H, N, d))
 
 
 def bwd(q, k, v, o, do, lse, causal: bool = False, scale: Optional[float] = None,
         workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None):
-    """dQ, dK, dV of the loss with gradient ``do`` w.r.t. O (d = 128)."""
-    B, H, N, d = _check_qkv(q, k, v, o, do)
+    """dQ, dK, dV of the loss with gradient ``do`` w.r.t. O (d = 128).  k, v
+    (and dk, dv) may have fewer heads than q (grouped query heads)."""
+    B, H, N, d = _check_qkv(q, o, do)
+    Hkv = _check_kv_heads(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     ws = bwd_workspace_bytes(B, H, N, d)
@@ -195,11 +232,19 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale: Optional[float] = None
     dv = torch.empty_like(v) if dv is None else dv
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
         raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    if dk.shape != k.shape or dv.shape != v.shape:
+        raise ValueError("dk, dv must have the shape of k, v")
     with torch.cuda.device(q.device):
-        st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                            _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H, N, d,
-                            int(bool(causal)), float(scale), _dtype_code(q), _stream(q))
-    _check(st, "attn_bwd")
+        if Hkv == H:
+            st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H, N,
+                                d, int(bool(causal)), float(scale), _dtype_code(q), _stream(q))
+        else:
+            st = lib().attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                    workspace.numel(), B, H, Hkv, N, d, int(bool(causal)),
+                                    float(scale), _dtype_code(q), _stream(q))
+    _check(st, "attn_bwd" if Hkv == H else "attn_bwd_gqa")
     return dq, dk, dv
 
 

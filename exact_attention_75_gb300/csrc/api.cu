@@ -122,6 +122,9 @@ attn_status fill_fwd_common(FwdLaunch* a, DeviceInfo* di, int B, int H, int N, f
   p.n_pairs = (p.n_qtiles + 1) / 2;
   p.n_kblocks = (N + 127) / 128;
   p.num_units = p.BH * p.n_pairs;
+  p.heads = H;
+  p.heads_kv = H;
+  p.group = 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = g_wait_limit_ns.load();
   a->num_ctas = di->num_sms;
@@ -135,11 +138,12 @@ using namespace attn;
 
 namespace {
 
-// attn_fwd with the keys cut into n_split runs of whole 128-key blocks, each
-// split writing its partial O / LSE at its own offset.
-attn_status fwd_split_impl(const void* q, const void* k, const void* v, void* o, float* lse,
-                           int n_split, int B, int H, int N, int d, int causal, float scale,
-                           attn_dtype dtype, void* stream) {
+// The forward pass with Hkv key/value heads for H query heads (Hkv = H: plain
+// multi-head attention) and the keys cut into n_split runs of whole 128-key
+// blocks, each split writing its partial O / LSE at its own offset.
+attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int n_split, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                     attn_dtype dtype, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
   if (n_split < 1 || n_split > 256) return ATTN_ERR_INVALID_ARG;
@@ -147,6 +151,7 @@ attn_status fwd_split_impl(const void* q, const void* k, const void* v, void* o,
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
@@ -155,13 +160,15 @@ attn_status fwd_split_impl(const void* q, const void* k, const void* v, void* o,
   FwdLaunch a;
   const CUtensorMapDataType dt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const int64_t BH = (int64_t)B * H;
+  const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
   if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmK, k, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmV, v, dt, 2, d, N, BH, 64, 128))
+      !encode_3d(&a.tmK, k, dt, 2, d, N, BHkv, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, BHkv, 64, 128))
     return ATTN_ERR_CUDA;
   fill_fwd_common(&a, di, B, H, N, scale, stream, o, lse);
   FwdParams& p = a.params;
+  p.heads_kv = Hkv;
+  p.group = H / Hkv;
   if ((int64_t)p.num_units * n_split > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
   p.n_split = n_split;
   p.num_units *= n_split;
@@ -202,14 +209,20 @@ attn_status attn_set_wait_limit_us(uint64_t limit_us) {
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int N, int d, int causal, float scale, attn_dtype dtype,
                      void* stream) {
-  return fwd_split_impl(q, k, v, o, lse, 1, B, H, N, d, causal, scale, dtype, stream);
+  return fwd_impl(q, k, v, o, lse, 1, B, H, H, N, d, causal, scale, dtype, stream);
+}
+
+attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         attn_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, 1, B, Hq, Hkv, N, d, causal, scale, dtype, stream);
 }
 
 attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_part,
                            float* lse_part, int n_split, int B, int H, int N, int d, int causal,
                            float scale, attn_dtype dtype, void* stream) {
-  return fwd_split_impl(q, k, v, o_part, lse_part, n_split, B, H, N, d, causal, scale, dtype,
-                        stream);
+  return fwd_impl(q, k, v, o_part, lse_part, n_split, B, H, H, N, d, causal, scale, dtype,
+                  stream);
 }
 
 attn_status attn_merge(const void* o_part, const float* lse_part, int n_split, void* o,
@@ -244,10 +257,10 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
   return (rows * 4 + 255) & ~(size_t)255;  // D = rowsum(dO o O), fp32
 }
 
-attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                     void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                     int causal, float scale, attn_dtype dtype, void* stream) {
+attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                         int d, int causal, float scale, attn_dtype dtype, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return ATTN_ERR_INVALID_ARG;
@@ -257,6 +270,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
@@ -266,10 +280,10 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   BwdLaunch a;
   const CUtensorMapDataType dt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const int64_t BH = (int64_t)B * H;
+  const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
   if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmK, k, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmV, v, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmK, k, dt, 2, d, N, BHkv, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, BHkv, 64, 128) ||
       !encode_3d(&a.tmDO, dout, dt, 2, d, N, BH, 64, 128))
     return ATTN_ERR_CUDA;
   BwdParams& p = a.params;
@@ -285,6 +299,10 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   p.delta = static_cast<float*>(workspace);
   p.status = di->status;
   p.BH = (int)BH;
+  p.BHkv = (int)BHkv;
+  p.heads = H;
+  p.heads_kv = Hkv;
+  p.group = H / Hkv;
   p.N = N;
   p.n_qtiles = (N + 127) / 128;
   p.n_kblocks = (N + 127) / 128;
@@ -297,6 +315,14 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   a.bf16 = dtype == ATTN_BF16;
   cudaError_t e = launch_bwd(a);
   return launch_result(e);
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                     int causal, float scale, attn_dtype dtype, void* stream) {
+  return attn_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H, N,
+                      d, causal, scale, dtype, stream);
 }
 
 attn_status attn_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales, int B, int H,

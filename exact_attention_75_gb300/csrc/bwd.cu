@@ -99,23 +99,38 @@ struct DkvLayout {
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
 struct DkvUnit {
-  int bh, j, i0, nsteps;
+  int bhkv;      // key/value head (batch * heads_kv + head)
+  int bhq0;      // first query head of its group
+  int j, i0;     // key tile; first query tile a query head sees
+  int per_head;  // steps per query head (query tiles i0 .. n_qtiles-1)
+  int nsteps;    // group * per_head
 };
+
+// Query head and query tile of step s of a unit: the group's query heads one
+// after another, each over its query tiles.
+__device__ __forceinline__ void dkv_step(const DkvUnit& w, int s, int* bhq, int* i) {
+  const int g = s / w.per_head;
+  *bhq = w.bhq0 + g;
+  *i = w.i0 + (s - g * w.per_head);
+}
 
 template <bool CAUSAL>
 __device__ __forceinline__ DkvUnit decode_dkv_unit(int u, const BwdParams& p) {
   DkvUnit w;
   if (CAUSAL) {
     // K/V tile j sees query tiles j..n-1: ascending j is longest first.
-    w.j = u / p.BH;
-    w.bh = u - w.j * p.BH;
+    w.j = u / p.BHkv;
+    w.bhkv = u - w.j * p.BHkv;
     w.i0 = w.j;
   } else {
-    w.bh = u / p.n_kblocks;
-    w.j = u - w.bh * p.n_kblocks;
+    w.bhkv = u / p.n_kblocks;
+    w.j = u - w.bhkv * p.n_kblocks;
     w.i0 = 0;
   }
-  w.nsteps = p.n_qtiles - w.i0;
+  const int b = w.bhkv / p.heads_kv;
+  w.bhq0 = b * p.heads + (w.bhkv - b * p.heads_kv) * p.group;
+  w.per_head = p.n_qtiles - w.i0;
+  w.nsteps = p.group * w.per_head;
   return w;
 }
 
@@ -171,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_holder;
   const int G = gridDim.x;
   const int cta = blockIdx.x;
-  const int num_units = p.BH * p.n_kblocks;
+  const int num_units = p.BHkv * p.n_kblocks;
 
   if (warp == kWarpProducer) {
     // -------------------------------------------------------------- producer ---
@@ -192,27 +207,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(L::kKvEmpty), (kv_it & 1) ^ 1, wd, 21);
         if (ok) {
           mbar_arrive_expect_tx(bar(L::kKvFull), 2 * kTile);
-          load_tile(sbase + L::kK, &tmK, bar(L::kKvFull), w.j * 128, w.bh);
-          load_tile(sbase + L::kV, &tmV, bar(L::kKvFull), w.j * 128, w.bh);
+          load_tile(sbase + L::kK, &tmK, bar(L::kKvFull), w.j * 128, w.bhkv);
+          load_tile(sbase + L::kV, &tmV, bar(L::kKvFull), w.j * 128, w.bhkv);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ++kv_it;
       for (int s = 0; s < w.nsteps && ok; ++s) {
-        const int i = w.i0 + s;
+        int bhq, i;
+        dkv_step(w, s, &bhq, &i);
         const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
         if (lane == 0) {
           ok = mbar_wait(bar(L::kQEmpty + qs), ((st_it / L::kQSlots) & 1) ^ 1, wd, 22);
           if (ok) {
             mbar_arrive_expect_tx(bar(L::kQFull + qs), kTile);
-            load_tile(sbase + L::kQ0 + qs * kTile, &tmQ, bar(L::kQFull + qs), i * 128, w.bh);
+            load_tile(sbase + L::kQ0 + qs * kTile, &tmQ, bar(L::kQFull + qs), i * 128, bhq);
             ++q_issued;
             ok = mbar_wait(bar(L::kDoEmpty + ds), ((st_it / L::kDoSlots) & 1) ^ 1, wd, 23);
           }
           if (ok) {
             mbar_arrive_expect_tx(bar(L::kDoFull + ds), kTile);
-            load_tile(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds), i * 128, w.bh);
+            load_tile(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds), i * 128, bhq);
             ++do_issued;
           }
         }
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int q = i * 128 + 4 * lane + e;
           const bool in = q < p.N;
-          const size_t g = (size_t)w.bh * p.N + (in ? q : 0);
+          const size_t g = (size_t)bhq * p.N + (in ? q : 0);
           l2[e] = in ? -p.lse[g] * kLog2e : -INFINITY;
           dd[e] = in ? -p.delta[g] : 0.f;
         }
@@ -364,7 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= num_units) break;
       const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
       for (int s = 0; s < w.nsteps; ++s) {
-        const int i = w.i0 + s;
+        int bhq, i;
+        dkv_step(w, s, &bhq, &i);
+        (void)bhq;
         const uint32_t ds = st_it % L::kDoSlots;
         const uint32_t par = st_it & 1;
         ok = mbar_wait(bar(L::kSFull), par, wd, 33);
@@ -471,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t src = tbase + lane_base + (h == 0 ? kColDV : kColDK);
       const float mult = (h == 0) ? 1.f : p.scale;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(h == 0 ? p.dv : p.dk) +
-                                            ((size_t)w.bh * p.N + key) * 128);
+                                            ((size_t)w.bhkv * p.N + key) * 128);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t raw[32];
@@ -528,6 +546,7 @@ constexpr uint32_t kColDQ = 0, kColS0 = 128, kColDP2 = 384;
 
 struct DqUnit {
   int bh, i, nsteps;
+  int bhkv;  // key/value head of query head bh
 };
 
 template <bool CAUSAL>
@@ -544,6 +563,8 @@ __device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
     w.i = u - w.bh * p.n_qtiles;
     w.nsteps = p.n_kblocks;
   }
+  const int b = w.bh / p.heads;
+  w.bhkv = b * p.heads_kv + (w.bh - b * p.heads) / p.group;
   return w;
 }
 
@@ -624,13 +645,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar(L::kKEmpty + ks), ((k_it / L::kKSlots) & 1) ^ 1, wd, 42);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kKFull + ks), kTile);
-          load_tile(sbase + L::kK0 + ks * kTile, &tmK, bar(L::kKFull + ks), j * 128, w.bh);
+          load_tile(sbase + L::kK0 + ks * kTile, &tmK, bar(L::kKFull + ks), j * 128, w.bhkv);
           ++k_it;
           const uint32_t vs = v_it % L::kVSlots;
           ok = mbar_wait(bar(L::kVEmpty + vs), ((v_it / L::kVSlots) & 1) ^ 1, wd, 43);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kVFull + vs), kTile);
-          load_tile(sbase + L::kV0 + vs * kTile, &tmV, bar(L::kVFull + vs), j * 128, w.bh);
+          load_tile(sbase + L::kV0 + vs * kTile, &tmV, bar(L::kVFull + vs), j * 128, w.bhkv);
           ++v_it;
         }
       }
@@ -919,7 +940,7 @@ template <bool CAUSAL, bool BF16>
 cudaError_t launch_main(const BwdLaunch& a) {
   static bool dkv_configured = false, dq_configured = false;
   cudaError_t e = launch_persistent(bwd_dkv_kernel<CAUSAL, BF16>, DkvLayout::kBytes,
-                                    &dkv_configured, a, a.params.BH * a.params.n_kblocks);
+                                    &dkv_configured, a, a.params.BHkv * a.params.n_kblocks);
   if (e != cudaSuccess) return e;
   return launch_persistent(bwd_dq_kernel<CAUSAL, BF16>, DqLayout::kBytes, &dq_configured, a,
                            a.params.BH * a.params.n_qtiles);

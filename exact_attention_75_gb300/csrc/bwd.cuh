@@ -19,7 +19,11 @@ struct BwdParams {
   void* dv;
   float* delta;          // workspace: D_i = sum_c dO_ic O_ic  [B*H, N]
   uint32_t* status;
-  int BH, N;
+  int BH, N;            // BH = B * heads (query heads)
+  // Grouped query heads: query head h of a batch uses key/value head
+  // h / group of its heads_kv; dK, dV ([B*heads_kv, N, D]) sum over the group.
+  int heads = 1, heads_kv = 1, group = 1;
+  int BHkv;              // B * heads_kv
   int n_qtiles;          // ceil(N / 128)
   int n_kblocks;         // ceil(N / 128)
   float scale;

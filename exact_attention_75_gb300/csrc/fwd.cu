@@ -74,6 +74,7 @@ struct FwdLayout {
 
 struct Unit {
   int bh, qp;
+  int bhkv;   // key/value head (batch * heads_kv + head / group)
   int split;  // key split of this unit (0 without a split)
   int kb0;    // first key block of the split
   int nb[2];  // K/V blocks visited by query tile 0 / 1 (0: tile absent or no key in the split)
@@ -95,6 +96,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     w.bh = u / p.n_pairs;
     w.qp = u - w.bh * p.n_pairs;
   }
+  const int b = w.bh / p.heads;
+  w.bhkv = b * p.heads_kv + (w.bh - b * p.heads) / p.group;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int tile = 2 * w.qp + t;
@@ -195,14 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (FP8) {
               // K: [128 keys][128 d] bytes; V^T: [128 d][128 keys] bytes.
               if (which == 0)
-                tma_load_3d(dst, &tmK, bar(L::kKvFull + slot), 0, (w.kb0 + j) * 128, w.bh);
+                tma_load_3d(dst, &tmK, bar(L::kKvFull + slot), 0, (w.kb0 + j) * 128, w.bhkv);
               else
-                tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), (w.kb0 + j) * 128, 0, w.bh);
+                tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), (w.kb0 + j) * 128, 0, w.bhkv);
             } else {
 #pragma unroll
               for (int h = 0; h < D / 64; ++h)
                 tma_load_3d(dst + h * 16384, which ? &tmV : &tmK, bar(L::kKvFull + slot),
-                            h * 64, (w.kb0 + j) * 128, w.bh);
+                            h * 64, (w.kb0 + j) * 128, w.bhkv);
             }
             ++kv_it;
           }
@@ -433,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* vsc = nullptr;
       if constexpr (FP8) {
         const size_t sb = (size_t)w.bh * p.n_sblocks;
-        ksc = p.k_scale + sb;
-        vsc = p.v_scale + sb;
+        ksc = p.k_scale + (size_t)w.bhkv * p.n_sblocks;
+        vsc = p.v_scale + (size_t)w.bhkv * p.n_sblocks;
         fq = p.q_scale[sb + min(row, p.N - 1) / 64] * sl2;
         float mv = 0.f;
         for (int b = lane; b < p.n_sblocks; b += 32) mv = fmaxf(mv, vsc[b]);

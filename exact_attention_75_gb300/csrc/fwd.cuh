@@ -21,6 +21,9 @@ struct FwdParams {
   // lse + s * lse_split (elements).  n_split = 1: the whole key range.
   int n_split = 1;
   size_t o_split = 0, lse_split = 0;
+  // Grouped query heads: BH counts query heads (B * heads); query head h of a
+  // batch uses key/value head h / group of the heads_kv of that batch.
+  int heads = 1, heads_kv = 1, group = 1;
   float scale_log2;     // scale * log2(e)
   unsigned long long wait_limit_ns;
   // E4M3 path only: per-(head, 64-row block) fp32 scales of Q, K and V.

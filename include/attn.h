@@ -71,6 +71,19 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      void* stream);
 
 /*
+ * Forward pass with grouped query heads (GQA; Hkv = 1 is multi-query
+ * attention): q, o [B,Hq,N,d], k, v [B,Hkv,N,d] with Hkv dividing Hq; query
+ * head h of a batch attends with key/value head h / (Hq/Hkv).  lse [B,Hq,N].
+ * Other arguments and errors as in attn_fwd (ATTN_ERR_INVALID_ARG if Hkv does
+ * not divide Hq).  attn_fwd is the case Hkv = Hq.
+ * Cite: the FlashAttention-2 review, "Insights" (linked work: GQA, training
+ * generalized multi-query transformer models).
+ */
+attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                         attn_dtype dtype, void* stream);
+
+/*
  * Forward pass over a split of the keys: the ceil(N/128) key blocks are cut
  * into n_split contiguous runs (split s = blocks [s nb / n_split,
  * (s+1) nb / n_split), a run may be empty), and split s writes the partial
@@ -134,6 +147,20 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const void* dout, const float* lse, void* dq, void* dk, void* dv,
                      void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                      int causal, float scale, attn_dtype dtype, void* stream);
+
+/*
+ * Backward pass with grouped query heads: q, o, dout, dq [B,Hq,N,d];
+ * k, v, dk, dv [B,Hkv,N,d]; lse [B,Hq,N]; Hkv divides Hq.  dK and dV of a
+ * key/value head sum the gradients of the query heads of its group (one CTA
+ * per key/value tile walks all of them, so the sum has a fixed order).
+ * workspace: >= attn_bwd_workspace_bytes(B, Hq, N, d).  Other arguments and
+ * errors as in attn_bwd; attn_bwd is the case Hkv = Hq.
+ * Cite: as attn_bwd, and the FlashAttention-2 review, "Insights" (GQA).
+ */
+attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,
+                         int d, int causal, float scale, attn_dtype dtype, void* stream);
 
 /*
  * Backward pass that allocates nothing (no counterpart on the pages: it is a
