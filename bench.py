@@ -292,6 +292,41 @@ def split_kv_timing(attn, st, w, stream, n_split, iters=20):
             "merge_bytes": merge_bytes}
 
 
+GQA_KV_HEADS = 4  # key/value heads of the grouped-query measurement
+
+
+def gqa_timing(attn, st, w, stream, hkv, iters=10):
+    """Forward + backward with grouped query heads on the step's workload
+    (H query heads, hkv key/value heads: the first head of each group of the
+    step's K, V, so no extra input draw), timed apart from the step."""
+    G = w.H // hkv
+    k = st.k[:, ::G].contiguous()
+    v = st.v[:, ::G].contiguous()
+    o, lse = attn.fwd(st.q, k, v, causal=w.causal)
+    grads = attn.bwd(st.q, k, v, o, st.do, lse, causal=w.causal)
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tf, tb = [], []
+    for _ in range(iters):
+        e[0].record(stream)
+        attn.fwd(st.q, k, v, causal=w.causal, out=o, lse=lse)
+        e[1].record(stream)
+        attn.bwd(st.q, k, v, o, st.do, lse, causal=w.causal, dq=grads[0], dk=grads[1],
+                 dv=grads[2])
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        tf.append(e[0].elapsed_time(e[1]))
+        tb.append(e[1].elapsed_time(e[2]))
+    status = attn.poll_status()
+    if status[0] != 0:
+        raise RuntimeError(f"device status after the GQA timing: {status}")
+    mf, mb = statistics.mean(tf), statistics.mean(tb)
+    return {"kv_heads": hkv, "fwd_ms": round(mf, 4), "bwd_ms": round(mb, 4),
+            "fwd_tflops": round(w.fwd_flops() / (mf * 1e-3) / 1e12, 1),
+            "bwd_tflops": round(w.bwd_flops() / (mb * 1e-3) / 1e12, 1),
+            "note": "grouped query heads, timed apart from the step (not in value)"}
+
+
 def run_gpu(args, rank, world, local_rank):
     import exact_attention_75_gb300 as attn
     dev = torch.device("cuda", local_rank)
@@ -374,12 +409,14 @@ def run_gpu(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     split = split_kv_timing(attn, st, w, stream, n_split=SPLIT_KV_N)
+    gqa = gqa_timing(attn, st, w, stream, GQA_KV_HEADS) if "bwd" in comps else None
 
     step_flops = sum(flops[c] for c in comps)
     ms_step = ms_total / args.steps
     if world > 1:
         ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
     return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks, split=split,
+                gqa=gqa,
                 flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
                 launches=sum(LAUNCHES[c] for c in comps) * args.steps)
 
@@ -511,6 +548,8 @@ def main():
                                 "frac": round(sp["merge_gbs"] / peaks["hbm_gbs"], 4),
                                 "algorithmic_bytes": mb}
         line["split_kv"] = sp
+    if r.get("gqa"):
+        line["gqa"] = r["gqa"]
     if not args.no_cpu_baseline:
         tf, dt, heads, cores = cpu_oracle_sample()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores,
