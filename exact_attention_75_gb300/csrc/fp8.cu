@@ -2,13 +2,24 @@
 // ("8.3 FlashAttention-3", section 5.1 block quantization and section 5.2
 // incoherent processing).
 //
-// One CTA per (batch*head, block of 64 rows); each warp owns 8 rows.  With the
-// rotation, every row x (d values) becomes (x H_d) o signs / sqrt(d) through
-// an in-register fast Walsh-Hadamard transform: lane l holds the d/32
-// consecutive values [l*d/32, (l+1)*d/32); butterflies of stride < d/32 stay
-// in registers, larger strides pair lanes with __shfl_xor_sync.  The block
-// scale is s = amax / 448 (one IEEE fp32 division; 1 for an all-zero block)
-// and the codes are E4M3(x / s), round to nearest even, saturating.
+// One CTA per (batch*head, block of 64 rows), 8 warps of 8 rows each; four
+// lanes share a row: lane (r = lane/4, q = lane%4) holds the d/4 values with
+// index 32k + 8q + j (k < d/32, j < 8), loaded as d/32 chunks of 16 bytes.
+//
+// Rotation: x R = (x H_d) diag(signs) / sqrt(d).  The fast Walsh-Hadamard
+// transform pairs index i with i ^ 2^b for every bit b; bits 0-2 and 5-6 are
+// register strides 1, 2, 4, 8, 16 (packed fp32x2 adds except stride 1), bits
+// 3-4 pair lanes through shuffles.  1/sqrt(d) is folded into the block's
+// quantization multiplier and the signs are applied to the codes (E4M3 is
+// sign-magnitude, so flipping bit 7 of a code negates it).
+//
+// Scale and codes: s = amax / 448 (one IEEE fp32 division; 1 for an all-zero
+// block), code = E4M3(RN(x / s)), round to nearest even, saturating.  Without
+// the rotation the codes are exact: t = RN(x * RN(1/s)) differs from x / s by
+// less than 3 units in the last place, E4M3 rounding is monotone, so when the
+// codes of t's neighbours 4 ulp below and above agree, that is the code of
+// RN(x / s); a thread with any disagreeing pair (rare, and every zero)
+// recomputes its codes with the IEEE division.
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -23,79 +34,103 @@ constexpr int kRowsPerBlock = 64;
 constexpr int kWarps = 8;
 constexpr float kE4M3Max = 448.f;
 
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// Codes of two values whose float bit patterns are moved by `delta` units in
+// the last place (towards zero for negative delta on the magnitude).
+__device__ __forceinline__ uint16_t codes_nudged(float2 t, int delta) {
+  return pack_e4m3x2(__uint_as_float(__float_as_uint(t.x) + (uint32_t)delta),
+                     __uint_as_float(__float_as_uint(t.y) + (uint32_t)delta));
+}
+
 template <int D, bool ROTATE, bool TRANSPOSED>
 __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const uint16_t* __restrict__ x,
                                                                uint8_t* __restrict__ out,
                                                                float* __restrict__ scales,
                                                                const int8_t* __restrict__ signs,
                                                                int N, int nblk) {
-  constexpr int E = D / 32;  // values per lane
-  constexpr int kRowsPerWarp = kRowsPerBlock / kWarps;
+  constexpr int K = D / 32;             // 16-byte chunks per lane
+  constexpr int E = 8 * K;              // values per lane
+  constexpr int W = 2 * K;              // code words (4 codes each) per lane
+  constexpr int kTileWords = D / 4 + 1; // staging row stride (transposed output)
   __shared__ float warp_max[kWarps];
-  __shared__ __align__(16) uint8_t tile[TRANSPOSED ? kRowsPerBlock * (D + 4) : 16];
+  __shared__ uint32_t tile[TRANSPOSED ? kRowsPerBlock * kTileWords : 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = lane & 3;
   const int bh = blockIdx.x / nblk;
   const int blk = blockIdx.x - bh * nblk;
   const int row0 = blk * kRowsPerBlock;
+  const int lrow = warp * 8 + (lane >> 2);
+  const int row = row0 + lrow;
+  const bool live = row < N;
 
-  float sgn[E];
-  if (ROTATE) {
-    const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+  float v[E];
+  {
+    uint4 raw[K];
+    const uint16_t* src = x + ((size_t)bh * N + (live ? row : 0)) * D + 8 * q;
 #pragma unroll
-    for (int e = 0; e < E; ++e) sgn[e] = (float)signs[lane * E + e] * inv_sqrt_d;
-  }
-
-  float v[kRowsPerWarp][E];
-  float amax = 0.f;
+    for (int k = 0; k < K; ++k)
+      raw[k] = live ? *reinterpret_cast<const uint4*>(src + 32 * k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-    const int row = row0 + warp * kRowsPerWarp + rr;
+    for (int k = 0; k < K; ++k) {
+      const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
-    for (int e = 0; e < E; ++e) v[rr][e] = 0.f;
-    if (row < N) {  // warp-uniform
-      const uint16_t* src = x + ((size_t)bh * N + row) * D + lane * E;
-      uint32_t w[E / 2];
-      if constexpr (E == 4) {
-        const uint2 t = *reinterpret_cast<const uint2*>(src);
-        w[0] = t.x;
-        w[1] = t.y;
-      } else {
-        w[0] = *reinterpret_cast<const uint32_t*>(src);
+      for (int i = 0; i < 4; ++i) {
+        v[8 * k + 2 * i] = __uint_as_float(w4[i] << 16);
+        v[8 * k + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
       }
-#pragma unroll
-      for (int e = 0; e < E / 2; ++e) {
-        v[rr][2 * e] = __uint_as_float(w[e] << 16);
-        v[rr][2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-      }
-      if (ROTATE) {
-        // in-register butterflies (strides 1 .. E/2)
-#pragma unroll
-        for (int s = 1; s < E; s <<= 1) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            if ((e & s) == 0) {
-              const float a = v[rr][e], b = v[rr][e + s];
-              v[rr][e] = a + b;
-              v[rr][e + s] = a - b;
-            }
-          }
-        }
-        // cross-lane butterflies (strides E .. D/2)
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[rr][e], m);
-            v[rr][e] = (lane & m) ? (o - v[rr][e]) : (v[rr][e] + o);
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[rr][e] *= sgn[e];
-      }
-#pragma unroll
-      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[rr][e]));
     }
   }
+
+  uint32_t flip[W];  // 0x80 in each byte whose sign is negative
+  if constexpr (ROTATE) {
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const int i0 = 32 * (w >> 1) + 8 * q + 4 * (w & 1);
+      uint32_t f = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) f |= (signs[i0 + b] < 0 ? 0x80u : 0u) << (8 * b);
+      flip[w] = f;
+    }
+    // register butterflies: stride 1 scalar, strides 2..E/2 on packed pairs
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float a = v[e], b = v[e + 1];
+      v[e] = a + b;
+      v[e + 1] = a - b;
+    }
+#pragma unroll
+    for (int st = 2; st < E; st <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        if ((e & st) == 0) {
+          const float2 a = f2(v[e], v[e + 1]), b = f2(v[e + st], v[e + st + 1]);
+          const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, f2(-1.f, -1.f), a);
+          v[e] = sum.x;
+          v[e + 1] = sum.y;
+          v[e + st] = dif.x;
+          v[e + st + 1] = dif.y;
+        }
+      }
+    }
+    // lane butterflies (index bits 3 and 4): the upper partner keeps o - v
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+      const float sl = (q & m) ? -1.f : 1.f;
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        const float o0 = __shfl_xor_sync(0xffffffffu, v[e], m);
+        const float o1 = __shfl_xor_sync(0xffffffffu, v[e + 1], m);
+        const float2 r = __ffma2_rn(f2(v[e], v[e + 1]), f2(sl, sl), f2(o0, o1));
+        v[e] = r.x;
+        v[e + 1] = r.y;
+      }
+    }
+  }
+
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) amax = fmax3(amax, fabsf(v[e]), fabsf(v[e + 1]));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -104,58 +139,74 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const uint16_t* _
   float bmax = warp_max[0];
 #pragma unroll
   for (int w2 = 1; w2 < kWarps; ++w2) bmax = fmaxf(bmax, warp_max[w2]);
+  // with the rotation, v is x H_d; the normalised block maximum is
+  // RN(max|x H_d| / sqrt(d)), the same as the maximum of the rounded values
+  const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+  if (ROTATE) bmax *= inv_sqrt_d;
   const float s = bmax > 0.f ? __fdiv_rn(bmax, kE4M3Max) : 1.0f;
   if (threadIdx.x == 0) scales[(size_t)bh * nblk + blk] = s;
 
+  uint32_t code[W];
+  const float mult = ROTATE ? __fdiv_rn(inv_sqrt_d, s) : __frcp_rn(s);
+  const float2 mult2 = f2(mult, mult);
+  bool agree = true;
 #pragma unroll
-  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-    const int lrow = warp * kRowsPerWarp + rr;
-    const int row = row0 + lrow;
-    uint32_t packed = 0;
+  for (int w = 0; w < W; ++w) {
+    uint32_t word = 0;
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const uint16_t two = pack_e4m3x2(__fdiv_rn(v[rr][e], s), __fdiv_rn(v[rr][e + 1], s));
-      packed |= (uint32_t)two << (8 * e);
-    }
-    if constexpr (!TRANSPOSED) {
-      if (row < N) {
-        uint8_t* dst = out + ((size_t)bh * N + row) * D + lane * E;
-        if constexpr (E == 4)
-          *reinterpret_cast<uint32_t*>(dst) = packed;
-        else
-          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+    for (int p = 0; p < 2; ++p) {
+      const int e = 4 * w + 2 * p;
+      const float2 t = __fmul2_rn(f2(v[e], v[e + 1]), mult2);
+      uint16_t two;
+      if constexpr (ROTATE) {
+        two = pack_e4m3x2(t.x, t.y);
+      } else {
+        two = codes_nudged(t, -4);
+        agree &= two == codes_nudged(t, 4);
       }
-    } else {
-      uint8_t* t = tile + lrow * (D + 4) + lane * E;
+      word |= (uint32_t)two << (16 * p);
+    }
+    code[w] = ROTATE ? word ^ flip[w] : word;
+  }
+  if (!ROTATE && !agree) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) t[e] = (uint8_t)(packed >> (8 * e));
+    for (int w = 0; w < W; ++w) {
+      const int e = 4 * w;
+      code[w] = (uint32_t)pack_e4m3x2(__fdiv_rn(v[e], s), __fdiv_rn(v[e + 1], s)) |
+                ((uint32_t)pack_e4m3x2(__fdiv_rn(v[e + 2], s), __fdiv_rn(v[e + 3], s)) << 16);
     }
   }
-  if constexpr (TRANSPOSED) {
-    // out is [bh][D][N]: column c of this row block becomes 64 contiguous
-    // bytes of output row c (rows at or beyond N are not written).
+
+  if constexpr (!TRANSPOSED) {
+    if (live) {
+      uint8_t* dst = out + ((size_t)bh * N + row) * D + 8 * q;
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        *reinterpret_cast<uint2*>(dst + 32 * k) = make_uint2(code[2 * k], code[2 * k + 1]);
+    }
+  } else {
+    // stage the codes row-major (word = 4 columns), then write out [bh][D][N]:
+    // a task takes 4 rows x 4 columns, transposes the 4x4 bytes and stores one
+    // word (4 consecutive rows) into each of the 4 output rows.
+#pragma unroll
+    for (int w = 0; w < W; ++w) tile[lrow * kTileWords + 8 * (w >> 1) + 2 * q + (w & 1)] = code[w];
     __syncthreads();
-    const int nrows = min(kRowsPerBlock, N - row0);
-    for (int idx = threadIdx.x; idx < D * 4; idx += blockDim.x) {
-      const int c = idx >> 2, part = idx & 3;  // 16 rows per part
-      uint32_t w4[4];
+    const int nrows = min(kRowsPerBlock, N - row0);  // a multiple of 16
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
+    for (int task = threadIdx.x; task < 16 * (D / 4); task += kWarps * 32) {
+      const int g = task & 15, cw = task >> 4;
+      if (4 * g >= nrows) continue;
+      const uint32_t a0 = tile[(4 * g + 0) * kTileWords + cw];
+      const uint32_t a1 = tile[(4 * g + 1) * kTileWords + cw];
+      const uint32_t a2 = tile[(4 * g + 2) * kTileWords + cw];
+      const uint32_t a3 = tile[(4 * g + 3) * kTileWords + cw];
+      const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
+      const uint32_t u0 = __byte_perm(a2, a3, 0x5140), u1 = __byte_perm(a2, a3, 0x7362);
+      const uint32_t col[4] = {__byte_perm(t0, u0, 0x5410), __byte_perm(t0, u0, 0x7632),
+                               __byte_perm(t1, u1, 0x5410), __byte_perm(t1, u1, 0x7632)};
+      uint8_t* dst = out + ((size_t)bh * D + 4 * cw) * N + row0 + 4 * g;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int lr = part * 16 + q * 4 + b;
-          word |= (uint32_t)tile[lr * (D + 4) + c] << (8 * b);
-        }
-        w4[q] = word;
-      }
-      uint8_t* dst = out + ((size_t)bh * D + c) * N + row0 + part * 16;
-      if (part * 16 + 16 <= nrows) {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      } else {
-        for (int b = 0; b < 16 && part * 16 + b < nrows; ++b)
-          dst[b] = (uint8_t)(w4[b >> 2] >> (8 * (b & 3)));
-      }
+      for (int b = 0; b < 4; ++b) *reinterpret_cast<uint32_t*>(dst + (size_t)b * N) = col[b];
     }
   }
 }
