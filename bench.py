@@ -327,6 +327,43 @@ def gqa_timing(attn, st, w, stream, hkv, iters=10):
             "note": "grouped query heads, timed apart from the step (not in value)"}
 
 
+def varlen_timing(attn, dev, stream, iters=10):
+    """Forward + backward on the packed variable-length batch (16 heads,
+    d = 128, bf16, causal, 16384 tokens per head in the seeded length mix),
+    timed apart from the step.  FLOPs per sequence of L rows and head: the
+    causal forward count 2 L^2 d, the backward 2.5x that."""
+    lengths = wl.varlen_lengths()
+    H, d = wl.VARLEN_HEADS, wl.VARLEN_D
+    inp = wl.make_varlen_inputs(lengths, H, H, d, "bf16", seed=0)
+    q, k, v, do, cu = (inp[n].to(dev) for n in ("q", "k", "v", "do", "cu_seqlens"))
+    mx = max(lengths)
+    o, lse = attn.fwd_varlen(q, k, v, cu, mx, causal=True)
+    grads = attn.bwd_varlen(q, k, v, o, do, lse, cu, mx, causal=True)
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tf, tb = [], []
+    for _ in range(iters):
+        e[0].record(stream)
+        attn.fwd_varlen(q, k, v, cu, mx, causal=True, out=o, lse=lse)
+        e[1].record(stream)
+        attn.bwd_varlen(q, k, v, o, do, lse, cu, mx, causal=True, dq=grads[0], dk=grads[1],
+                        dv=grads[2])
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        tf.append(e[0].elapsed_time(e[1]))
+        tb.append(e[1].elapsed_time(e[2]))
+    status = attn.poll_status()
+    if status[0] != 0:
+        raise RuntimeError(f"device status after the variable-length timing: {status}")
+    ff = sum(2.0 * H * n * n * d for n in lengths)
+    mf, mb = statistics.mean(tf), statistics.mean(tb)
+    return {"lengths": lengths, "heads": H, "d": d, "fwd_ms": round(mf, 4),
+            "bwd_ms": round(mb, 4), "fwd_tflops": round(ff / (mf * 1e-3) / 1e12, 1),
+            "bwd_tflops": round(2.5 * ff / (mb * 1e-3) / 1e12, 1),
+            "note": "packed variable-length batch (causal per sequence), timed apart from "
+                    "the step (not in value)"}
+
+
 def run_gpu(args, rank, world, local_rank):
     import exact_attention_75_gb300 as attn
     dev = torch.device("cuda", local_rank)
@@ -410,13 +447,14 @@ def run_gpu(args, rank, world, local_rank):
 
     split = split_kv_timing(attn, st, w, stream, n_split=SPLIT_KV_N)
     gqa = gqa_timing(attn, st, w, stream, GQA_KV_HEADS) if "bwd" in comps else None
+    varlen = varlen_timing(attn, dev, stream) if "bwd" in comps else None
 
     step_flops = sum(flops[c] for c in comps)
     ms_step = ms_total / args.steps
     if world > 1:
         ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
     return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks, split=split,
-                gqa=gqa,
+                gqa=gqa, varlen=varlen,
                 flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
                 launches=sum(LAUNCHES[c] for c in comps) * args.steps)
 
@@ -550,6 +588,8 @@ def main():
         line["split_kv"] = sp
     if r.get("gqa"):
         line["gqa"] = r["gqa"]
+    if r.get("varlen"):
+        line["varlen"] = r["varlen"]
     if not args.no_cpu_baseline:
         tf, dt, heads, cores = cpu_oracle_sample()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores,

@@ -19,8 +19,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["AttnError", "lib", "lib_path", "fwd", "fwd_split", "merge", "bwd",
-           "bwd_workspace_bytes", "quantize_fp8", "fwd_fp8", "poll_status", "set_wait_limit_us",
+__all__ = ["AttnError", "lib", "lib_path", "fwd", "fwd_split", "merge", "bwd", "fwd_varlen",
+           "bwd_varlen", "bwd_workspace_bytes", "quantize_fp8", "fwd_fp8", "poll_status", "set_wait_limit_us",
            "selftest_wait_timeout", "num_sms", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         "attn_fwd_gqa": ([vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp], i),
         "attn_bwd_gqa": ([vp] * 10 + [sz, i, i, i, i, i, i, f, i, vp], i),
         "attn_merge": ([vp, vp, i, vp, vp, i, i, i, i, i, vp], i),
+        "attn_fwd_varlen": ([vp] * 6 + [i, i, i, i, i, i, i, f, i, vp], i),
+        "attn_bwd_varlen": ([vp] * 10 + [sz, vp, i, i, i, i, i, i, i, f, i, vp], i),
         "attn_bwd_workspace_bytes": ([i, i, i, i], sz),
         "attn_bwd": ([vp] * 10 + [sz, i, i, i, i, i, f, i, vp], i),
         "attn_quantize_fp8": ([vp, vp, vp, i, i, i, i, i, vp, i, vp], i),
@@ -312,6 +314,82 @@ def selftest_wait_timeout(limit_us: int = 20000, device=None) -> Tuple[int, int]
     st = lib().attn_selftest_wait_timeout(int(limit_us), ctypes.c_void_p(s.cuda_stream),
                                           ctypes.byref(detail))
     return int(st), int(detail.value)
+
+
+def _check_varlen(q, k, v, cu_seqlens, max_seqlen, *more) -> Tuple[int, int, int, int, int]:
+    """Shapes of a packed variable-length batch: q (and more) [H, total, d],
+    k, v [Hkv, total, d], cu_seqlens int32 [n_seq + 1] on q's device."""
+    if q.dim() != 3:
+        raise ValueError("packed tensors must be [H, total, d]")
+    H, T, d = q.shape
+    if k.dim() != 3 or k.shape != v.shape or k.shape[1:] != q.shape[1:]:
+        raise ValueError("k, v must be [Hkv, total, d] with q's total and d")
+    if H % k.shape[0] != 0:
+        raise ValueError("the number of key/value heads must divide the query heads")
+    for t in (q, k, v) + more:
+        if not t.is_cuda or t.device != q.device or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, dO must be contiguous CUDA tensors of one dtype")
+    for t in more:
+        if t.shape != q.shape:
+            raise ValueError("o and dO must have q's shape")
+    if (cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2
+            or cu_seqlens.device != q.device or not cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous int32 [n_seq + 1] tensor on q's device")
+    if not 1 <= int(max_seqlen) <= T:
+        raise ValueError("max_seqlen must lie in [1, total]")
+    return H, int(k.shape[0]), T, d, cu_seqlens.numel() - 1
+
+
+def fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+               max_seqlen: int, causal: bool = False, scale: Optional[float] = None,
+               out: Optional[torch.Tensor] = None,
+               lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention over a packed batch of sequences of their own lengths.
+    q [H, total, d], k, v [Hkv, total, d]; sequence b is rows
+    cu_seqlens[b]..cu_seqlens[b+1] and attends only to itself.  Returns
+    O [H, total, d] and LSE [H, total] fp32.  max_seqlen >= every length."""
+    H, Hkv, T, d, n_seq = _check_varlen(q, k, v, cu_seqlens, max_seqlen)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    _check_varlen(q, k, v, cu_seqlens, max_seqlen, out)
+    if tuple(lse.shape) != (H, T) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, total] tensor")
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                   _ptr(cu_seqlens), n_seq, int(max_seqlen), T, H, Hkv, d,
+                                   int(bool(causal)), float(scale), _dtype_code(q), _stream(q))
+    _check(st, "attn_fwd_varlen")
+    return out, lse
+
+
+def bwd_varlen(q, k, v, o, do, lse, cu_seqlens: torch.Tensor, max_seqlen: int,
+               causal: bool = False, scale: Optional[float] = None,
+               workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None):
+    """dQ, dK, dV of fwd_varlen (d = 128); layouts as fwd_varlen."""
+    H, Hkv, T, d, n_seq = _check_varlen(q, k, v, cu_seqlens, max_seqlen, o, do)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if tuple(lse.shape) != (H, T) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, total] tensor")
+    ws = bwd_workspace_bytes(1, H, T, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dq.shape != q.shape or dk.shape != k.shape or dv.shape != v.shape:
+        raise ValueError("dq, dk, dv must have the shapes of q, k, v")
+    with torch.cuda.device(q.device):
+        st = lib().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                   workspace.numel(), _ptr(cu_seqlens), n_seq, int(max_seqlen),
+                                   T, H, Hkv, d, int(bool(causal)), float(scale),
+                                   _dtype_code(q), _stream(q))
+    _check(st, "attn_bwd_varlen")
+    return dq, dk, dv
 
 
 def num_sms() -> int:

@@ -100,6 +100,43 @@ bool encode_3d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int esiz
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Host-side checks of a variable-length batch description (the offsets
+// themselves live on the device and are checked there).
+bool varlen_args_ok(const int* cu_seqlens, int n_seq, int max_seqlen, int total) {
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3) != 0) return false;
+  if (n_seq < 1 || total < 1) return false;
+  return max_seqlen >= 1 && max_seqlen <= total;
+}
+
+// Records ATTN_ERR_INVALID_ARG (site 60, the first bad index in the block
+// field) in the status word unless cu_seqlens[0] = 0, cu_seqlens[n_seq] =
+// total and 0 <= cu_seqlens[b+1] - cu_seqlens[b] <= max_seqlen for every b.
+// The attention kernels clamp every sequence into [0, total) themselves, so
+// a bad array gives wrong numbers but no access outside the tensors.
+__global__ void varlen_check_kernel(const int* cu, int n_seq, int total, int max_seqlen,
+                                    uint32_t* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b > n_seq) return;
+  bool bad = false;
+  if (b == 0) bad = cu[0] != 0;
+  if (b == n_seq) bad = bad || cu[n_seq] != total;
+  if (b < n_seq) {
+    const int len = cu[b + 1] - cu[b];
+    bad = bad || len < 0 || len > max_seqlen;
+  }
+  if (bad)
+    atomicCAS(status, 0u, (uint32_t)ATTN_ERR_INVALID_ARG | (60u << 8) |
+                              ((uint32_t)min(b, 0xFFFF) << 16));
+}
+
+cudaError_t launch_varlen_check(const int* cu, int n_seq, int total, int max_seqlen,
+                                uint32_t* status, cudaStream_t stream) {
+  const int threads = 256;
+  const int blocks = (n_seq + 1 + threads - 1) / threads;
+  varlen_check_kernel<<<blocks, threads, 0, stream>>>(cu, n_seq, total, max_seqlen, status);
+  return cudaGetLastError();
+}
+
 bool shape_ok(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return false;
   if (d != 64 && d != 128) return false;
@@ -141,11 +178,19 @@ namespace {
 // The forward pass with Hkv key/value heads for H query heads (Hkv = H: plain
 // multi-head attention) and the keys cut into n_split runs of whole 128-key
 // blocks, each split writing its partial O / LSE at its own offset.
+//
+// With cu_seqlens (device, B + 1 entries) the batch is B packed sequences of
+// at most max_seqlen rows: q, o are [H, N, d], k, v [Hkv, N, d], lse [H, N],
+// N the total rows.
 attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                      int n_split, int B, int H, int Hkv, int N, int d, int causal, float scale,
-                     attn_dtype dtype, void* stream) {
+                     attn_dtype dtype, void* stream, const int* cu_seqlens = nullptr,
+                     int max_seqlen = 0) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
+  const bool varlen = cu_seqlens != nullptr;
+  if (varlen && !varlen_args_ok(cu_seqlens, B, max_seqlen, N)) return ATTN_ERR_INVALID_ARG;
+  if (varlen && n_split != 1) return ATTN_ERR_INVALID_ARG;
   if (n_split < 1 || n_split > 256) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
@@ -161,14 +206,28 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   const CUtensorMapDataType dt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
-  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmK, k, dt, 2, d, N, BHkv, 64, 128) ||
-      !encode_3d(&a.tmV, v, dt, 2, d, N, BHkv, 64, 128))
+  // tensor-map head index: (batch, head) for dense tensors, head for packed ones
+  const int64_t zq = varlen ? H : BH, zkv = varlen ? Hkv : BHkv;
+  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, zq, 64, 128) ||
+      !encode_3d(&a.tmK, k, dt, 2, d, N, zkv, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, zkv, 64, 128))
     return ATTN_ERR_CUDA;
   fill_fwd_common(&a, di, B, H, N, scale, stream, o, lse);
   FwdParams& p = a.params;
   p.heads_kv = Hkv;
   p.group = H / Hkv;
+  if (varlen) {
+    p.cu_seqlens = cu_seqlens;
+    p.max_seqlen = max_seqlen;
+    p.n_qtiles = (max_seqlen + 127) / 128;
+    p.n_kblocks = p.n_qtiles;
+    p.n_pairs = (p.n_qtiles + 1) / 2;
+    if ((int64_t)p.BH * p.n_pairs > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
+    p.num_units = p.BH * p.n_pairs;
+    cudaError_t e = launch_varlen_check(cu_seqlens, B, N, max_seqlen, di->status,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return launch_result(e);
+  }
   if ((int64_t)p.num_units * n_split > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
   p.n_split = n_split;
   p.num_units *= n_split;
@@ -257,10 +316,19 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
   return (rows * 4 + 255) & ~(size_t)255;  // D = rowsum(dO o O), fp32
 }
 
-attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
-                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                         void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
-                         int d, int causal, float scale, attn_dtype dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward pass; with cu_seqlens the packed variable-length layout of
+// fwd_impl (dq like q, dk / dv like k / v).
+attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                     int d, int causal, float scale, attn_dtype dtype, void* stream,
+                     const int* cu_seqlens = nullptr, int max_seqlen = 0) {
+  const bool varlen = cu_seqlens != nullptr;
+  if (varlen && !varlen_args_ok(cu_seqlens, B, max_seqlen, N)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return ATTN_ERR_INVALID_ARG;
@@ -273,7 +341,8 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
   if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
-  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_workspace_bytes(varlen ? 1 : B, H, N, d))
+    return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
   if (st != ATTN_OK) return st;
@@ -281,10 +350,11 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
   const CUtensorMapDataType dt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
-  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
-      !encode_3d(&a.tmK, k, dt, 2, d, N, BHkv, 64, 128) ||
-      !encode_3d(&a.tmV, v, dt, 2, d, N, BHkv, 64, 128) ||
-      !encode_3d(&a.tmDO, dout, dt, 2, d, N, BH, 64, 128))
+  const int64_t zq = varlen ? H : BH, zkv = varlen ? Hkv : BHkv;
+  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, zq, 64, 128) ||
+      !encode_3d(&a.tmK, k, dt, 2, d, N, zkv, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, zkv, 64, 128) ||
+      !encode_3d(&a.tmDO, dout, dt, 2, d, N, zq, 64, 128))
     return ATTN_ERR_CUDA;
   BwdParams& p = a.params;
   p.q = q;
@@ -306,6 +376,13 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
   p.N = N;
   p.n_qtiles = (N + 127) / 128;
   p.n_kblocks = (N + 127) / 128;
+  if (varlen) {
+    p.cu_seqlens = cu_seqlens;
+    p.max_seqlen = max_seqlen;
+    p.n_qtiles = (max_seqlen + 127) / 128;
+    p.n_kblocks = p.n_qtiles;
+    if ((int64_t)p.BH * p.n_qtiles > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
+  }
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = g_wait_limit_ns.load();
@@ -313,8 +390,43 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
   a.stream = static_cast<cudaStream_t>(stream);
   a.causal = causal != 0;
   a.bf16 = dtype == ATTN_BF16;
+  if (varlen) {
+    cudaError_t e = launch_varlen_check(cu_seqlens, B, N, max_seqlen, di->status, a.stream);
+    if (e != cudaSuccess) return launch_result(e);
+  }
   cudaError_t e = launch_bwd(a);
   return launch_result(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                         int d, int causal, float scale, attn_dtype dtype, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d,
+                  causal, scale, dtype, stream);
+}
+
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens, int n_seq, int max_seqlen, int total, int Hq,
+                            int Hkv, int d, int causal, float scale, attn_dtype dtype,
+                            void* stream) {
+  if (cu_seqlens == nullptr) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, 1, n_seq, Hq, Hkv, total, d, causal, scale, dtype, stream,
+                  cu_seqlens, max_seqlen);
+}
+
+attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, const int* cu_seqlens,
+                            int n_seq, int max_seqlen, int total, int Hq, int Hkv, int d,
+                            int causal, float scale, attn_dtype dtype, void* stream) {
+  if (cu_seqlens == nullptr) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, n_seq, Hq, Hkv,
+                  total, d, causal, scale, dtype, stream, cu_seqlens, max_seqlen);
 }
 
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -397,7 +509,9 @@ attn_status attn_poll_device_status(void* stream, uint32_t* detail) {
     const uint32_t zero = 0;
     if (cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    return (word & 0xFF) == kStatusTimeout ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA;
+    const uint32_t code = word & 0xFF;
+    if (code == kStatusTimeout) return ATTN_ERR_TIMEOUT;
+    return code == ATTN_ERR_INVALID_ARG ? ATTN_ERR_INVALID_ARG : ATTN_ERR_CUDA;
   }
   return ATTN_OK;
 }

@@ -98,38 +98,63 @@ struct DkvLayout {
 // dS^T those of dP^T.
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
-struct DkvUnit {
-  int bhkv;      // key/value head (batch * heads_kv + head)
-  int bhq0;      // first query head of its group
-  int j, i0;     // key tile; first query tile a query head sees
-  int per_head;  // steps per query head (query tiles i0 .. n_qtiles-1)
-  int nsteps;    // group * per_head
+// Rows of sequence b: [row0, row0 + len) of every head.  Dense batches are
+// one sequence of N rows per (batch, head) tensor-map index.
+struct SeqRows {
+  int row0, len;
 };
 
-// Query head and query tile of step s of a unit: the group's query heads one
-// after another, each over its query tiles.
-__device__ __forceinline__ void dkv_step(const DkvUnit& w, int s, int* bhq, int* i) {
+__device__ __forceinline__ SeqRows seq_rows(const BwdParams& p, int b) {
+  if (p.cu_seqlens == nullptr) return SeqRows{0, p.N};
+  // clamped into [0, N] so that no access leaves the tensors
+  const int s0 = min(max(__ldg(p.cu_seqlens + b), 0), p.N);
+  const int s1 = min(max(__ldg(p.cu_seqlens + b + 1), s0), p.N);
+  return SeqRows{s0, min(s1 - s0, p.max_seqlen)};
+}
+
+struct DkvUnit {
+  int bhkv;      // key/value head (batch * heads_kv + head)
+  int zkv, zq0;  // tensor-map index of the K/V head and of its group's first query head
+  int row0, len; // the sequence's rows
+  int j, i0;     // key tile; first query tile a query head sees
+  int per_head;  // steps per query head (query tiles i0 .. end of the sequence)
+  int nsteps;    // group * per_head (0: the key tile lies past the sequence's end)
+};
+
+// Tensor-map index of the query head and query tile of step s of a unit: the
+// group's query heads one after another, each over its query tiles.
+__device__ __forceinline__ void dkv_step(const DkvUnit& w, int s, int* zq, int* i) {
   const int g = s / w.per_head;
-  *bhq = w.bhq0 + g;
+  *zq = w.zq0 + g;
   *i = w.i0 + (s - g * w.per_head);
 }
 
 template <bool CAUSAL>
 __device__ __forceinline__ DkvUnit decode_dkv_unit(int u, const BwdParams& p) {
   DkvUnit w;
-  if (CAUSAL) {
+  if (CAUSAL || p.cu_seqlens != nullptr) {
     // K/V tile j sees query tiles j..n-1: ascending j is longest first.
     w.j = u / p.BHkv;
     w.bhkv = u - w.j * p.BHkv;
-    w.i0 = w.j;
   } else {
     w.bhkv = u / p.n_kblocks;
     w.j = u - w.bhkv * p.n_kblocks;
-    w.i0 = 0;
   }
+  w.i0 = CAUSAL ? w.j : 0;
   const int b = w.bhkv / p.heads_kv;
-  w.bhq0 = b * p.heads + (w.bhkv - b * p.heads_kv) * p.group;
-  w.per_head = p.n_qtiles - w.i0;
+  const int hkv = w.bhkv - b * p.heads_kv;
+  const SeqRows sr = seq_rows(p, b);
+  w.row0 = sr.row0;
+  w.len = sr.len;
+  if (p.cu_seqlens != nullptr) {
+    w.zkv = hkv;
+    w.zq0 = hkv * p.group;
+  } else {
+    w.zkv = w.bhkv;
+    w.zq0 = b * p.heads + hkv * p.group;
+  }
+  const int nt = (w.len + 127) >> 7;
+  w.per_head = w.j < nt ? nt - w.i0 : 0;
   w.nsteps = p.group * w.per_head;
   return w;
 }
@@ -203,32 +228,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = snake_unit(k, cta, G);
       if (u >= num_units) break;
       const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
+      if (w.nsteps == 0) continue;
       if (lane == 0) {
         ok = mbar_wait(bar(L::kKvEmpty), (kv_it & 1) ^ 1, wd, 21);
         if (ok) {
           mbar_arrive_expect_tx(bar(L::kKvFull), 2 * kTile);
-          load_tile(sbase + L::kK, &tmK, bar(L::kKvFull), w.j * 128, w.bhkv);
-          load_tile(sbase + L::kV, &tmV, bar(L::kKvFull), w.j * 128, w.bhkv);
+          load_tile(sbase + L::kK, &tmK, bar(L::kKvFull), w.row0 + w.j * 128, w.zkv);
+          load_tile(sbase + L::kV, &tmV, bar(L::kKvFull), w.row0 + w.j * 128, w.zkv);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ++kv_it;
       for (int s = 0; s < w.nsteps && ok; ++s) {
-        int bhq, i;
-        dkv_step(w, s, &bhq, &i);
+        int zq, i;
+        dkv_step(w, s, &zq, &i);
         const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
         if (lane == 0) {
           ok = mbar_wait(bar(L::kQEmpty + qs), ((st_it / L::kQSlots) & 1) ^ 1, wd, 22);
           if (ok) {
             mbar_arrive_expect_tx(bar(L::kQFull + qs), kTile);
-            load_tile(sbase + L::kQ0 + qs * kTile, &tmQ, bar(L::kQFull + qs), i * 128, bhq);
+            load_tile(sbase + L::kQ0 + qs * kTile, &tmQ, bar(L::kQFull + qs),
+                      w.row0 + i * 128, zq);
             ++q_issued;
             ok = mbar_wait(bar(L::kDoEmpty + ds), ((st_it / L::kDoSlots) & 1) ^ 1, wd, 23);
           }
           if (ok) {
             mbar_arrive_expect_tx(bar(L::kDoFull + ds), kTile);
-            load_tile(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds), i * 128, bhq);
+            load_tile(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds),
+                      w.row0 + i * 128, zq);
             ++do_issued;
           }
         }
@@ -240,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int q = i * 128 + 4 * lane + e;
-          const bool in = q < p.N;
-          const size_t g = (size_t)bhq * p.N + (in ? q : 0);
+          const bool in = q < w.len;
+          const size_t g = (size_t)zq * p.N + w.row0 + (in ? q : 0);
           l2[e] = in ? -p.lse[g] * kLog2e : -INFINITY;
           dd[e] = in ? -p.delta[g] : 0.f;
         }
@@ -295,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = snake_unit(k, cta, G);
         if (u >= num_units) break;
         const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
+        if (w.nsteps == 0) continue;
         ok = mbar_wait(bar(L::kKvFull), kv_it & 1, wd, 25);
         if (!ok) break;
         ++kv_it;
@@ -379,10 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = snake_unit(k, cta, G);
       if (u >= num_units) break;
       const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
+      if (w.nsteps == 0) continue;
       for (int s = 0; s < w.nsteps; ++s) {
-        int bhq, i;
-        dkv_step(w, s, &bhq, &i);
-        (void)bhq;
+        int zq, i;
+        dkv_step(w, s, &zq, &i);
+        (void)zq;
         const uint32_t ds = st_it % L::kDoSlots;
         const uint32_t par = st_it & 1;
         ok = mbar_wait(bar(L::kSFull), par, wd, 33);
@@ -489,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t src = tbase + lane_base + (h == 0 ? kColDV : kColDK);
       const float mult = (h == 0) ? 1.f : p.scale;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(h == 0 ? p.dv : p.dk) +
-                                            ((size_t)w.bhkv * p.N + key) * 128);
+                                            ((size_t)w.zkv * p.N + w.row0 + key) * 128);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t raw[32];
@@ -499,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e)
           pk[e] = pack16x2(BF16, __uint_as_float(raw[2 * e]) * mult,
                            __uint_as_float(raw[2 * e + 1]) * mult);
-        if (key < p.N) {
+        if (key < w.len) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[4 * c + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -545,26 +575,37 @@ struct DqLayout {
 constexpr uint32_t kColDQ = 0, kColS0 = 128, kColDP2 = 384;
 
 struct DqUnit {
-  int bh, i, nsteps;
-  int bhkv;  // key/value head of query head bh
+  int bh, i, nsteps;  // nsteps = 0: the query tile lies past the sequence's end
+  int zq, zkv;        // tensor-map index of the query head and of its K/V head
+  int row0, len;      // the sequence's rows
 };
 
 template <bool CAUSAL>
 __device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
   DqUnit w;
-  if (CAUSAL) {
+  if (CAUSAL || p.cu_seqlens != nullptr) {
     // Query tile i sees key tiles 0..i: descending i is longest first.
     const int r = u / p.BH;
     w.bh = u - r * p.BH;
     w.i = p.n_qtiles - 1 - r;
-    w.nsteps = min(w.i + 1, p.n_kblocks);
   } else {
     w.bh = u / p.n_qtiles;
     w.i = u - w.bh * p.n_qtiles;
-    w.nsteps = p.n_kblocks;
   }
   const int b = w.bh / p.heads;
-  w.bhkv = b * p.heads_kv + (w.bh - b * p.heads) / p.group;
+  const int hq = w.bh - b * p.heads;
+  const SeqRows sr = seq_rows(p, b);
+  w.row0 = sr.row0;
+  w.len = sr.len;
+  if (p.cu_seqlens != nullptr) {
+    w.zq = hq;
+    w.zkv = hq / p.group;
+  } else {
+    w.zq = w.bh;
+    w.zkv = b * p.heads_kv + hq / p.group;
+  }
+  const int nt = (w.len + 127) >> 7;
+  w.nsteps = w.i < nt ? (CAUSAL ? w.i + 1 : nt) : 0;
   return w;
 }
 
@@ -634,24 +675,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = snake_unit(k, cta, G);
         if (u >= num_units) break;
         const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
+        if (w.nsteps == 0) continue;
         ok = mbar_wait(bar(L::kQEmpty), (unit_it & 1) ^ 1, wd, 41);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kQFull), 2 * kTile);
-        load_tile(sbase + L::kQ, &tmQ, bar(L::kQFull), w.i * 128, w.bh);
-        load_tile(sbase + L::kDO, &tmDO, bar(L::kQFull), w.i * 128, w.bh);
+        load_tile(sbase + L::kQ, &tmQ, bar(L::kQFull), w.row0 + w.i * 128, w.zq);
+        load_tile(sbase + L::kDO, &tmDO, bar(L::kQFull), w.row0 + w.i * 128, w.zq);
         ++unit_it;
         for (int j = 0; j < w.nsteps && ok; ++j) {
           const uint32_t ks = k_it % L::kKSlots;
           ok = mbar_wait(bar(L::kKEmpty + ks), ((k_it / L::kKSlots) & 1) ^ 1, wd, 42);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kKFull + ks), kTile);
-          load_tile(sbase + L::kK0 + ks * kTile, &tmK, bar(L::kKFull + ks), j * 128, w.bhkv);
+          load_tile(sbase + L::kK0 + ks * kTile, &tmK, bar(L::kKFull + ks), w.row0 + j * 128,
+                    w.zkv);
           ++k_it;
           const uint32_t vs = v_it % L::kVSlots;
           ok = mbar_wait(bar(L::kVEmpty + vs), ((v_it / L::kVSlots) & 1) ^ 1, wd, 43);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kVFull + vs), kTile);
-          load_tile(sbase + L::kV0 + vs * kTile, &tmV, bar(L::kVFull + vs), j * 128, w.bhkv);
+          load_tile(sbase + L::kV0 + vs * kTile, &tmV, bar(L::kVFull + vs), w.row0 + j * 128,
+                    w.zkv);
           ++v_it;
         }
       }
@@ -690,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = snake_unit(k, cta, G);
         if (u >= num_units) break;
         const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
+        if (w.nsteps == 0) continue;
         ok = mbar_wait(bar(L::kQFull), unit_it & 1, wd, 45);
         if (!ok) break;
         tc_fence_after();
@@ -776,9 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = snake_unit(k, cta, G);
       if (u >= num_units) break;
       const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
+      if (w.nsteps == 0) continue;
       const int row = w.i * 128 + r;
-      const bool in = row < p.N;
-      const size_t grow = (size_t)w.bh * p.N + (in ? row : 0);
+      const bool in = row < w.len;
+      const size_t grow = (size_t)w.zq * p.N + w.row0 + (in ? row : 0);
       // Padding rows: LSE = +inf, D = 0, so their P and dS vanish.
       const float nl2 = in ? -p.lse[grow] * kLog2e : -INFINITY;
       const float nd = in ? -p.delta[grow] : 0.f;
@@ -816,6 +862,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int col = 0; col < 64; ++col)  // key column within the half
               if (64 * h + col > r) pr[col] = 0.f;  // key after query
+          }
+          // keys past the sequence's end (zero-filled or another sequence's)
+          const int kend = w.len - j * 128 - 64 * h;
+          if (kend < 64) {
+#pragma unroll
+            for (int col = 0; col < 64; ++col)
+              if (col >= kend) pr[col] = 0.f;
           }
         }
         // ---- dS = P o (dP - D)
@@ -949,7 +1002,9 @@ cudaError_t launch_main(const BwdLaunch& a) {
 template <bool BF16>
 cudaError_t launch_all(const BwdLaunch& a) {
   const BwdParams& p = a.params;
-  const long rows = (long)p.BH * p.N;
+  // rows of O / dO: every (batch, head) holds N, a packed variable-length
+  // batch holds N per head
+  const long rows = (long)(p.cu_seqlens != nullptr ? p.heads : p.BH) * p.N;
   long blocks = (rows + 7) / 8;
   const long cap = (long)a.num_sms * 16;
   if (blocks > cap) blocks = cap;

@@ -24,6 +24,13 @@ struct BwdParams {
   // h / group of its heads_kv; dK, dV ([B*heads_kv, N, D]) sum over the group.
   int heads = 1, heads_kv = 1, group = 1;
   int BHkv;              // B * heads_kv
+  // Variable-length batch (cu_seqlens non-null): q, o, dO, dQ are
+  // [heads, N, D], k, v, dK, dV [heads_kv, N, D] and lse, delta [heads, N],
+  // with N the total rows; sequence b owns rows [cu_seqlens[b],
+  // cu_seqlens[b+1]) of every head.  B counts sequences, n_qtiles and
+  // n_kblocks count tiles of max_seqlen; units past a sequence's end are empty.
+  const int* cu_seqlens = nullptr;
+  int max_seqlen = 0;
   int n_qtiles;          // ceil(N / 128)
   int n_kblocks;         // ceil(N / 128)
   float scale;

@@ -75,6 +75,10 @@ struct FwdLayout {
 struct Unit {
   int bh, qp;
   int bhkv;   // key/value head (batch * heads_kv + head / group)
+  int zq, zkv;  // tensor-map head index of Q / O and of K / V
+  int row0;   // first row of the sequence in its head
+  int len;    // rows of the sequence
+  int nkb;    // its 128-row tiles (query tiles = key blocks)
   int split;  // key split of this unit (0 without a split)
   int kb0;    // first key block of the split
   int nb[2];  // K/V blocks visited by query tile 0 / 1 (0: tile absent or no key in the split)
@@ -85,9 +89,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   Unit w;
   w.split = u % p.n_split;  // splits of one query-tile pair are neighbours
   u /= p.n_split;
-  w.kb0 = (w.split * p.n_kblocks) / p.n_split;
-  const int kb1 = ((w.split + 1) * p.n_kblocks) / p.n_split;
-  if (CAUSAL) {
+  if (CAUSAL || p.cu_seqlens != nullptr) {
     // Longest first: the heaviest query-tile pairs of every head come first.
     const int r = u / p.BH;
     w.bh = u - r * p.BH;
@@ -97,14 +99,33 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     w.qp = u - w.bh * p.n_pairs;
   }
   const int b = w.bh / p.heads;
-  w.bhkv = b * p.heads_kv + (w.bh - b * p.heads) / p.group;
+  const int hq = w.bh - b * p.heads;
+  if (p.cu_seqlens != nullptr) {
+    // rows clamped into [0, N] so that no access leaves the tensors
+    const int s0 = min(max(__ldg(p.cu_seqlens + b), 0), p.N);
+    const int s1 = min(max(__ldg(p.cu_seqlens + b + 1), s0), p.N);
+    w.row0 = s0;
+    w.len = min(s1 - s0, p.max_seqlen);
+    w.zq = hq;
+    w.zkv = hq / p.group;
+    w.bhkv = w.zkv;
+  } else {
+    w.row0 = 0;
+    w.len = p.N;
+    w.zq = w.bh;
+    w.bhkv = b * p.heads_kv + hq / p.group;
+    w.zkv = w.bhkv;
+  }
+  w.nkb = (w.len + 127) >> 7;
+  w.kb0 = (w.split * w.nkb) / p.n_split;
+  const int kb1 = ((w.split + 1) * w.nkb) / p.n_split;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int tile = 2 * w.qp + t;
-    if (tile >= p.n_qtiles) {
+    if (tile >= w.nkb) {
       w.nb[t] = 0;
     } else {
-      const int visible = CAUSAL ? min(tile + 1, p.n_kblocks) : p.n_kblocks;
+      const int visible = CAUSAL ? min(tile + 1, w.nkb) : w.nkb;
       w.nb[t] = max(0, min(visible, kb1) - w.kb0);
     }
   }
@@ -177,12 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
           const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
           if constexpr (FP8) {
-            tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, (2 * w.qp + t) * 128, w.bh);
+            tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, w.row0 + (2 * w.qp + t) * 128, w.zq);
           } else {
 #pragma unroll
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(dst + h * 16384, &tmQ, bar(L::kQFull + t), h * 64,
-                          (2 * w.qp + t) * 128, w.bh);
+                          w.row0 + (2 * w.qp + t) * 128, w.zq);
           }
           ++q_it[t];
         }
@@ -198,14 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (FP8) {
               // K: [128 keys][128 d] bytes; V^T: [128 d][128 keys] bytes.
               if (which == 0)
-                tma_load_3d(dst, &tmK, bar(L::kKvFull + slot), 0, (w.kb0 + j) * 128, w.bhkv);
+                tma_load_3d(dst, &tmK, bar(L::kKvFull + slot), 0, (w.kb0 + j) * 128, w.zkv);
               else
-                tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), (w.kb0 + j) * 128, 0, w.bhkv);
+                tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), (w.kb0 + j) * 128, 0, w.zkv);
             } else {
 #pragma unroll
               for (int h = 0; h < D / 64; ++h)
                 tma_load_3d(dst + h * 16384, which ? &tmV : &tmK, bar(L::kKvFull + slot),
-                            h * 64, (w.kb0 + j) * 128, w.bhkv);
+                            h * 64, w.row0 + (w.kb0 + j) * 128, w.zkv);
             }
             ++kv_it;
           }
@@ -418,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* const lbase = p.lse + w.split * p.lse_split;
       if (nb == 0) {
         // A query tile that sees no key of this split: O = 0, LSE = -inf.
-        if (tile < p.n_qtiles && row < p.N) {
-          const size_t grow = (size_t)w.bh * p.N + row;
+        if (tile < w.nkb && row < w.len) {
+          const size_t grow = (size_t)w.zq * p.N + w.row0 + row;
           uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -487,10 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int jk = w.kb0 + j;  // key block index
         const bool diag = CAUSAL && (jk == tile);
-        const bool tail = (jk == p.n_kblocks - 1) && (p.N & 127);
+        const bool tail = (jk == w.nkb - 1) && (w.len & 127);
         if (diag || tail) {
           const int kbase = jk * 128;
-          const int lim = CAUSAL ? min(row, p.N - 1) : (p.N - 1);
+          const int lim = CAUSAL ? min(row, w.len - 1) : (w.len - 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
@@ -583,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (aborted) continue;
       tc_fence_after();
       const float inv_l = (FP8 ? sv_max : 1.0f) / l;
-      const size_t grow = (size_t)w.bh * p.N + row;
+      const size_t grow = (size_t)w.zq * p.N + w.row0 + row;
       uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -596,13 +617,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float b = __uint_as_float(raw[2 * i + 1]) * inv_l;
           pk[i] = (BF16 || FP8) ? pack_bf16x2(a, b) : pack_f16x2(a, b);
         }
-        if (row < p.N) {
+        if (row < w.len) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             orow[c * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (row < p.N) lbase[grow] = (m + log2f(l)) * 0.69314718055994530942f;
+      if (row < w.len) lbase[grow] = (m + log2f(l)) * 0.69314718055994530942f;
       tc_fence_before();
     }
   }

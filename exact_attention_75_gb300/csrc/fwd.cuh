@@ -24,6 +24,13 @@ struct FwdParams {
   // Grouped query heads: BH counts query heads (B * heads); query head h of a
   // batch uses key/value head h / group of the heads_kv of that batch.
   int heads = 1, heads_kv = 1, group = 1;
+  // Variable-length batch (cu_seqlens non-null): q, o are [heads, N, D] and
+  // k, v [heads_kv, N, D] with N the total rows of all sequences; sequence b
+  // owns rows [cu_seqlens[b], cu_seqlens[b+1]) of every head and attends only
+  // within itself.  BH = n_seq * heads; n_qtiles, n_kblocks and n_pairs count
+  // tiles of max_seqlen, and units past a shorter sequence's end are empty.
+  const int* cu_seqlens = nullptr;
+  int max_seqlen = 0;
   float scale_log2;     // scale * log2(e)
   unsigned long long wait_limit_ns;
   // E4M3 path only: per-(head, 64-row block) fp32 scales of Q, K and V.

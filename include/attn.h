@@ -163,6 +163,46 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
                          int d, int causal, float scale, attn_dtype dtype, void* stream);
 
 /*
+ * Variable-length batch: n_seq independent sequences of different lengths,
+ * packed back to back.  Sequence b owns rows [cu_seqlens[b], cu_seqlens[b+1])
+ * of every head and attends only to its own keys (causal: key index <= query
+ * index, both counted from the sequence's first row).
+ *   q, o       : [Hq, total, d] fp16/bf16 (head-major, rows packed).
+ *   k, v       : [Hkv, total, d];  Hkv divides Hq (query head h uses h/(Hq/Hkv)).
+ *   lse        : [Hq, total] fp32, written.
+ *   cu_seqlens : DEVICE array of n_seq + 1 int32, cu_seqlens[0] = 0,
+ *                cu_seqlens[n_seq] = total, non-decreasing (empty sequences
+ *                allowed), 4-byte aligned, read only.
+ *   max_seqlen : >= the longest sequence, <= total; it sizes the launch.
+ * The offsets are checked on the device: a violation records
+ * ATTN_ERR_INVALID_ARG in the status word (attn_poll_device_status returns
+ * it; the block field of `detail` holds the first bad index).  Every
+ * sequence is clamped into [0, total) and to max_seqlen rows, so a bad array
+ * gives wrong results but no access outside the tensors.  d in {64, 128}.
+ * Cite: the FlashAttention-2 review, "Discussion Points" (the decoding /
+ * KV-cache access pattern: many sequences of their own lengths); per
+ * sequence the computation is attn_fwd's.
+ */
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens, int n_seq, int max_seqlen, int total, int Hq,
+                            int Hkv, int d, int causal, float scale, attn_dtype dtype,
+                            void* stream);
+
+/*
+ * Backward pass of attn_fwd_varlen: q, o, dout, dq [Hq, total, d]; k, v, dk,
+ * dv [Hkv, total, d]; lse [Hq, total] from attn_fwd_varlen.  workspace: >=
+ * attn_bwd_workspace_bytes(1, Hq, total, d) bytes, 256-byte aligned.  Rows of
+ * dq, dk, dv outside every sequence (none when the offsets are valid) are
+ * not written.  d = 128.  Offsets, checks and errors as in attn_fwd_varlen.
+ * Cite: as attn_bwd and attn_fwd_varlen.
+ */
+attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, const int* cu_seqlens,
+                            int n_seq, int max_seqlen, int total, int Hq, int Hkv, int d,
+                            int causal, float scale, attn_dtype dtype, void* stream);
+
+/*
  * Backward pass that allocates nothing (no counterpart on the pages: it is a
  * library convenience, not part of the method).
  *
@@ -226,8 +266,9 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const 
  * word.  Returns ATTN_ERR_TIMEOUT if a kernel pipeline wait ran out of time
  * since the last poll (the kernel then skipped the rest of its work and
  * released its resources; outputs are incomplete), ATTN_ERR_CUDA if the
- * synchronisation failed, else ATTN_OK.  `detail` (may be NULL) receives the
- * raw status word: code | wait-site << 8 | block index << 16.
+ * synchronisation failed, ATTN_ERR_INVALID_ARG if a device-side argument
+ * check failed (variable-length offsets), else ATTN_OK.  `detail` (may be
+ * NULL) receives the raw status word: code | site << 8 | block index << 16.
  */
 attn_status attn_poll_device_status(void* stream, uint32_t* detail);
 

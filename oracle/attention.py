@@ -49,7 +49,8 @@ __all__ = [
     "attention_backward", "E4M3_MAX", "e4m3_decode", "e4m3_encode", "hadamard_matrix",
     "rotation_matrix", "quantize_blocks", "dequantize_blocks", "rmse",
     "split_key_ranges", "attention_partial_head", "attention_split", "merge_partials",
-    "kv_head_of", "attention_gqa", "attention_backward_gqa",
+    "kv_head_of", "attention_gqa", "attention_backward_gqa", "sequence_ranges",
+    "attention_varlen", "attention_backward_varlen",
 ]
 
 
@@ -257,6 +258,64 @@ def attention_backward_gqa(q, k, v, do, causal: bool, scale: float):
             dQ[b, h] = dq
             dK[b, g] += dk
             dV[b, g] += dv
+    return dQ, dK, dV
+
+
+# ---------------------------------------------------------------------------
+# Variable-length batches: independent sequences packed back to back
+# ---------------------------------------------------------------------------
+# [FA2-review] "Discussion Points" asks about many sequences, each with its
+# own length (the decoding / KV-cache access pattern).  Plainest reading: each
+# sequence is its own attention problem, the plain definition over its rows,
+# with the causal diagonal counted from the sequence's first row.  Rows
+# [cu[b], cu[b+1]) of every head belong to sequence b.
+
+def sequence_ranges(cu_seqlens):
+    """[(lo, hi)] row ranges of the sequences of a packed batch."""
+    cu = [int(c) for c in np.asarray(cu_seqlens).ravel()]
+    assert cu[0] == 0 and all(b >= a for a, b in zip(cu, cu[1:]))
+    return list(zip(cu[:-1], cu[1:]))
+
+
+def attention_varlen(q, k, v, cu_seqlens, causal: bool, scale: float):
+    """q: [Hq,T,d], k, v: [Hkv,T,d] -> O [Hq,T,d], LSE [Hq,T] (rows outside
+    every sequence stay NaN)."""
+    q = np.asarray(q, np.float64)
+    Hq, T, d = q.shape
+    Hkv = np.shape(k)[0]
+    O = np.full((Hq, T, np.shape(v)[-1]), np.nan)
+    L = np.full((Hq, T), np.nan)
+    for lo, hi in sequence_ranges(cu_seqlens):
+        if hi == lo:
+            continue
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            O[h, lo:hi], L[h, lo:hi], _ = attention_head(q[h, lo:hi], k[g, lo:hi], v[g, lo:hi],
+                                                         causal, scale)
+    return O, L
+
+
+def attention_backward_varlen(q, k, v, do, cu_seqlens, causal: bool, scale: float):
+    """dQ [Hq,T,d], dK / dV [Hkv,T,d] of attention_varlen: per sequence and
+    query head the plain backward; dK, dV summed over each group."""
+    q = np.asarray(q, np.float64)
+    Hq, T, d = q.shape
+    Hkv = np.shape(k)[0]
+    dQ = np.full(q.shape, np.nan)
+    dK = np.full((Hkv,) + np.shape(k)[1:], np.nan)
+    dV = np.full((Hkv,) + np.shape(v)[1:], np.nan)
+    for lo, hi in sequence_ranges(cu_seqlens):
+        if hi == lo:
+            continue
+        dK[:, lo:hi] = 0.0
+        dV[:, lo:hi] = 0.0
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            dq, dk, dv, _ = attention_backward_head(q[h, lo:hi], k[g, lo:hi], v[g, lo:hi],
+                                                    do[h, lo:hi], causal, scale)
+            dQ[h, lo:hi] = dq
+            dK[g, lo:hi] += dk
+            dV[g, lo:hi] += dv
     return dQ, dK, dV
 
 

@@ -497,3 +497,90 @@ def test_kv_head_mapping_is_contiguous_groups():
     assert [oracle.kv_head_of(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
     assert [oracle.kv_head_of(h, 4, 1) for h in range(4)] == [0, 0, 0, 0]
     assert [oracle.kv_head_of(h, 4, 4) for h in range(4)] == [0, 1, 2, 3]
+
+
+# ---------------------------------------------------------------------------
+# Variable-length batches (sequences packed back to back; "Discussion Points"
+# of [FA2-review]).  Pins: attention over all packed rows with a
+# block-diagonal (and, causal, per-sequence lower-triangular) mask built
+# directly from the offsets; sequences do not see one another; the gradient
+# by finite differences, an empty sequence included.
+# ---------------------------------------------------------------------------
+
+def _block_diagonal_mask(cu, causal):
+    T = int(cu[-1])
+    seq = np.full(T, -1)
+    for b in range(len(cu) - 1):
+        seq[cu[b]:cu[b + 1]] = b
+    pos = np.arange(T) - np.asarray(cu)[np.maximum(seq, 0)]
+    allowed = seq[:, None] == seq[None, :]
+    if causal:
+        allowed &= pos[None, :] <= pos[:, None]
+    return allowed
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 2), (3, 1)])
+def test_varlen_equals_block_diagonal_masked_attention(causal, Hq, Hkv):
+    rng = np.random.default_rng(7 * Hq + Hkv + causal)
+    cu = np.array([0, 5, 5, 12, 13, 21])  # lengths 5, 0, 7, 1, 8
+    T, d = int(cu[-1]), 6
+    q = rng.standard_normal((Hq, T, d))
+    k, v = (rng.standard_normal((Hkv, T, d)) for _ in range(2))
+    O, L = oracle.attention_varlen(q, k, v, cu, causal, 0.5)
+    allowed = _block_diagonal_mask(cu, causal)
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        S = 0.5 * q[h] @ k[g].T
+        S = np.where(allowed, S, -np.inf)
+        m = S.max(axis=1, keepdims=True)
+        e = np.exp(S - m)
+        assert np.allclose(O[h], (e / e.sum(axis=1, keepdims=True)) @ v[g], rtol=0, atol=1e-13)
+        assert np.allclose(L[h], np.log(e.sum(axis=1)) + m[:, 0], rtol=0, atol=1e-13)
+
+
+def test_varlen_sequences_are_isolated():
+    rng = np.random.default_rng(3)
+    cu = np.array([0, 9, 20, 26])
+    q, k, v = (rng.standard_normal((2, 26, 4)) for _ in range(3))
+    O, L = oracle.attention_varlen(q, k, v, cu, True, 0.7)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, 9:20] = rng.standard_normal((2, 11, 4))
+    v2[:, 9:20] = rng.standard_normal((2, 11, 4))
+    O2, L2 = oracle.attention_varlen(q, k2, v2, cu, True, 0.7)
+    for lo, hi in [(0, 9), (20, 26)]:
+        assert np.array_equal(O[:, lo:hi], O2[:, lo:hi]) and np.array_equal(L[:, lo:hi],
+                                                                            L2[:, lo:hi])
+    assert not np.allclose(O[:, 9:20], O2[:, 9:20])
+    # the first row of every sequence sees only its own key under the causal mask
+    for lo in (0, 9, 20):
+        assert np.allclose(O[:, lo], v[:, lo], atol=1e-15)
+
+
+def test_varlen_gradient_by_finite_differences():
+    rng = np.random.default_rng(29)
+    cu = np.array([0, 3, 3, 7])  # lengths 3, 0, 4
+    q = rng.standard_normal((4, 7, 3))
+    k, v = (rng.standard_normal((2, 7, 3)) for _ in range(2))
+    do = rng.standard_normal(q.shape)
+    dQ, dK, dV = oracle.attention_backward_varlen(q, k, v, do, cu, True, 0.6)
+
+    def loss(qq, kk, vv):
+        O, _ = oracle.attention_varlen(qq, kk, vv, cu, True, 0.6)
+        return float(np.sum(O * do))
+
+    eps = 1e-6
+    for (h, i, c) in [(0, 0, 1), (3, 6, 2), (2, 4, 0), (1, 2, 2)]:
+        qp, qm = q.copy(), q.copy()
+        qp[h, i, c] += eps
+        qm[h, i, c] -= eps
+        assert abs((loss(qp, k, v) - loss(qm, k, v)) / (2 * eps) - dQ[h, i, c]) < 1e-7
+    for (g, i, c) in [(0, 3, 1), (1, 6, 2), (1, 0, 0), (0, 2, 2)]:
+        kp, km = k.copy(), k.copy()
+        kp[g, i, c] += eps
+        km[g, i, c] -= eps
+        assert abs((loss(q, kp, v) - loss(q, km, v)) / (2 * eps) - dK[g, i, c]) < 1e-7
+        vp, vm = v.copy(), v.copy()
+        vp[g, i, c] += eps
+        vm[g, i, c] -= eps
+        assert abs((loss(q, k, vp) - loss(q, k, vm)) / (2 * eps) - dV[g, i, c]) < 1e-7

@@ -126,6 +126,44 @@ def make_inputs(w: Workload, with_do: Optional[bool] = None) -> Dict[str, torch.
     return out
 
 
+# Variable-length batch measured beside the dense step: 16 heads, d = 128,
+# bf16, causal, the same 16384 tokens per head as the dense [2,16,8192,128]
+# workload, cut into sequences whose lengths are drawn uniformly from
+# [VARLEN_MIN, VARLEN_MAX] (seed 0; the last one is cut to fill the total).
+VARLEN_TOTAL, VARLEN_MIN, VARLEN_MAX, VARLEN_HEADS, VARLEN_D = 16384, 256, 4096, 16, 128
+
+
+def varlen_lengths(total: int = VARLEN_TOTAL, lo: int = VARLEN_MIN, hi: int = VARLEN_MAX,
+                   seed: int = 0) -> List[int]:
+    """Sequence lengths drawn uniformly from [lo, hi] until they sum to total."""
+    g = torch.Generator().manual_seed(seed)
+    out: List[int] = []
+    while sum(out) < total:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g))
+        out.append(min(n, total - sum(out)))
+    return out
+
+
+def make_varlen_inputs(lengths: List[int], Hq: int, Hkv: int, d: int, dtype: str,
+                       seed: int = 0, with_do: bool = True) -> Dict[str, torch.Tensor]:
+    """Packed inputs of a variable-length batch on the CPU: q (and do)
+    [Hq, T, d], k, v [Hkv, T, d] fp32 standard normals drawn in the order q,
+    k, v, do and cast to ``dtype``; ``cu_seqlens`` int32 [n+1] (row offsets)."""
+    g = torch.Generator().manual_seed(seed)
+    T = int(sum(lengths))
+    tdt = {"fp16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    shapes = {"q": (Hq, T, d), "k": (Hkv, T, d), "v": (Hkv, T, d)}
+    if with_do:
+        shapes["do"] = (Hq, T, d)
+    out = {n: torch.randn(sh, generator=g, dtype=torch.float32).to(tdt)
+           for n, sh in shapes.items()}
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    out["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32)
+    return out
+
+
 def head_range(rank: int, world: int, BH: int) -> range:
     """Contiguous share of the B*H independent heads given to ``rank``."""
     per = (BH + world - 1) // world
