@@ -24,12 +24,15 @@
 // accumulator in tensor memory; P and dS feed the dV / dK / dQ products
 // from tensor memory.
 //
-// CTA organisation of both kernels (320 threads):
+// CTA organisation (bwd_dkv 320 threads, bwd_dq 352):
 //   warps 0-3 / 4-7  compute warpgroups, one per half of the 128 columns of
 //                    S (query columns in bwd_dkv, key columns in bwd_dq);
 //                    thread = TMEM lane = row
 //   warp 8           TMA producer
 //   warp 9           tcgen05 issuer + tensor-memory owner
+//   warp 10          (bwd_dq) relay: waits on the pipeline's mbarriers and
+//                    meets the issuer at a named barrier, so that the issuer
+//                    never touches shared memory between its commits
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -43,9 +46,12 @@ namespace attn {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;    // bwd_dkv
+constexpr int kThreadsDq = 352;  // bwd_dq (+ relay warp)
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpRelay = 10;
+constexpr uint32_t kBarRelay = 3;  // named barrier: relay warp + issuer warp (64 threads)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStatusLayout = 5;  // shared memory not 1024-byte aligned
 constexpr int kTile = 32768;           // 128 x 128 16-bit values
@@ -552,27 +558,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // K_j is read by S_j and, one step later, by dQ_j; V_j only by dP_j.  Each
 // gets a ring sized to its lifetime (3 K slots, 2 V slots) so a slot's next
-// load has about two steps of MMA work to land in.
+// load has about two steps of MMA work to land in.  Q_i and dO_i land here
+// and are copied into tensor memory once per unit, so the S and dP MMAs read
+// only K_j / V_j from shared memory.
 struct DqLayout {
-  static constexpr int kQ = 0;                    // Q_i (K-major A of S = Q K^T)
-  static constexpr int kDO = kTile;               // dO_i (K-major A of dP = dO V^T)
+  static constexpr int kQ = 0;                    // Q_i staging (K-major)
+  static constexpr int kDO = kTile;               // dO_i staging (K-major)
   static constexpr int kKSlots = 3, kVSlots = 2;
   static constexpr int kK0 = 2 * kTile;           // K ring
   static constexpr int kV0 = kK0 + kKSlots * kTile;  // V ring
   static constexpr int kBar = kV0 + kVSlots * kTile;
   enum {
     kQFull, kQEmpty, kKFull, kKEmpty = kKFull + kKSlots, kVFull = kKEmpty + kKSlots,
-    kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots, kDpFull = kSFull + 2, kDsReady,
-    kDqFull, kDqFree, kDrain, kNumBars
+    kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots, kSRead = kSFull + 2, kDpFull,
+    kDsReady, kDqFull, kDqFree, kDrain, kNumBars
   };
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static_assert(kBytes <= 232448, "shared memory budget (227 KB) exceeded");
 };
 
-// Tensor memory: dQ [0,128)  S (two buffers) [128,256) [256,384)  dP [384,512);
-// dS (16-bit) of warpgroup h overwrites dP columns [384+64h, 384+64h+32).
-constexpr uint32_t kColDQ = 0, kColS0 = 128, kColDP2 = 384;
+// Tensor memory: dQ [0,128)  two step buffers [128,256) [256,384)  Q_i
+// [384,448)  dO_i [448,512) (16-bit, two values per column: the A operands of
+// S and dP).  Step j uses buffer j%2 for S_j, then (once S_j has been read)
+// for dP_j; dS_j (16-bit) of warpgroup h overwrites its columns
+// [64h, 64h+32) after dP_j has been read.
+constexpr uint32_t kColDQ = 0, kColS0 = 128, kColQ = 384, kColDO = 448;
 
 struct DqUnit {
   int bh, i, nsteps;  // nsteps = 0: the query tile lies past the sequence's end
@@ -610,7 +621,7 @@ __device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
 }
 
 template <bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsDq, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdParams p) {
@@ -643,6 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kVEmpty + s), 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(bar(L::kSFull + s), 1);
+    mbar_init(bar(L::kSRead), 256);
     mbar_init(bar(L::kDpFull), 1);
     mbar_init(bar(L::kDsReady), 256);
     mbar_init(bar(L::kDqFull), 1);
@@ -713,106 +725,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ tcgen05 issuer ---
-    // Per step j: S_j into buffer j%2 | dQ += dS_{j-1} K_{j-1} | dP_j.  The
-    // warpgroups compute P_j while dQ and dP_j run, and dS_j while S_{j+1}
-    // runs.
-    if (lane == 0) {
+    // Per unit: Q_i, dO_i copied into tensor memory.  Per step j (buffer
+    // b = j%2): S_j into b | dQ += dS_{j-1} K_{j-1} | dP_j into b once the
+    // warpgroups have read S_j.  The warpgroups compute P_j while dQ and dP_j
+    // run, and dS_j while S_{j+1} runs.  Each group is issued after a
+    // rendezvous with the relay warp, which has seen its inputs complete.
+    // After an abort both warps still walk the whole schedule (issuing
+    // nothing), so every rendezvous pairs up.
+    {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);  // S, dP
       constexpr uint32_t kIdQ = idesc_f16(128, 128, BF16, false, true);   // dQ
-      uint32_t k_it = 0, v_it = 0, unit_it = 0, step_it = 0;
-      bool ok = true;
+      uint32_t k_it = 0, v_it = 0, step_it = 0;
+      bool aborted = false;
       const uint64_t qd = kmajor_base(sbase + L::kQ), dod = kmajor_base(sbase + L::kDO);
-      // dQ += dS K_j: A = dS from tensor memory, B = K_j read MN-major.
-      auto issue_dq = [&](uint32_t kaddr, uint32_t acc0) {
+      // dQ += dS K_j: A = dS from tensor memory (buffer sb), B = K_j read MN-major.
+      auto issue_dq = [&](uint32_t kaddr, uint32_t sb, uint32_t acc0) {
         const uint64_t kd_mn = mnmajor_base(kaddr);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ts(tbase + kColDQ, tbase + kColDP2 + half_packed_col(kk),
+          mma_f16_ts(tbase + kColDQ, tbase + kColS0 + 128 * sb + half_packed_col(kk),
                      desc_plus(kd_mn, mnmajor16_off(kk)), kIdQ, kk > 0 ? 1u : acc0);
       };
-      for (int k = 0; ok; ++k) {
+      for (int k = 0;; ++k) {
         const int u = snake_unit(k, cta, G);
         if (u >= num_units) break;
         const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
-        ok = mbar_wait(bar(L::kQFull), unit_it & 1, wd, 45);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t prev_kaddr = 0, prev_ks = 0;
-        for (int j = 0; j < w.nsteps && ok; ++j) {
+        uint32_t prev_kaddr = 0, prev_ks = 0, prev_sb = 0;
+        for (int j = 0; j < w.nsteps; ++j) {
           const uint32_t ks = k_it % L::kKSlots;
-          ok = mbar_wait(bar(L::kKFull + ks), (k_it / L::kKSlots) & 1, wd, 46);
-          if (!ok) break;
-          tc_fence_after();
           const uint32_t kaddr = sbase + L::kK0 + ks * kTile;
           const uint32_t sb = step_it & 1;
-          // S_j = Q_i K_j^T into buffer sb (its previous S was read before
-          // the dS it produced was handed over, which the previous dQ awaited).
-          const uint64_t kd = kmajor_base(kaddr);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + kColS0 + 128 * sb, desc_plus(qd, kmajor16_off(kk)),
-                       desc_plus(kd, kmajor16_off(kk)), kIdS, kk > 0);
-          mma_commit(bar(L::kSFull + sb));
-          if (j > 0) {
-            // dQ += dS_{j-1} K_{j-1}
-            ok = mbar_wait(bar(L::kDsReady), (step_it - 1) & 1, wd, 47);
-            if (!ok) break;
-            if (j == 1 && unit_it > 0) {  // the previous unit's dQ has been stored
-              ok = mbar_wait(bar(L::kDqFree), (unit_it - 1) & 1, wd, 48);
-              if (!ok) break;
-            }
+          // K_j (and at j = 0 Q_i, dO_i) have landed
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+          if (!aborted && lane == 0) {
             tc_fence_after();
-            issue_dq(prev_kaddr, j > 1 ? 1u : 0u);
-            mma_commit(bar(L::kKEmpty + prev_ks));
-          }
-          // dP_j = dO_i V_j^T (dS_{j-1} in these columns has just been consumed)
-          const uint32_t vs = v_it % L::kVSlots;
-          ok = mbar_wait(bar(L::kVFull + vs), (v_it / L::kVSlots) & 1, wd, 55);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vd = kmajor_base(sbase + L::kV0 + vs * kTile);
+            if (j == 0) {
+              // Q_i, dO_i into tensor memory, 16 columns of d per copy.  The
+              // previous unit's S and dP (their last readers) have completed:
+              // the dS that the last dQ awaited was computed from them.
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + kColDP2, desc_plus(dod, kmajor16_off(kk)),
-                       desc_plus(vd, kmajor16_off(kk)), kIdS, kk > 0);
-          mma_commit(bar(L::kDpFull));
-          mma_commit(bar(L::kVEmpty + vs));
-          if (j == w.nsteps - 1) mma_commit(bar(L::kQEmpty));  // Q_i, dO_i no longer read
+              for (int kk = 0; kk < 8; ++kk) {
+                tmem_cp_128x256b(tbase + kColQ + 8 * kk, desc_plus(qd, kmajor16_off(kk)));
+                tmem_cp_128x256b(tbase + kColDO + 8 * kk, desc_plus(dod, kmajor16_off(kk)));
+              }
+              mma_commit(bar(L::kQEmpty));  // the staging tiles may be reloaded
+            }
+            // S_j = Q_i K_j^T into buffer sb (its previous contents, dS_{j-2},
+            // were read by dQ_{j-2}, issued before).
+            const uint64_t kd = kmajor_base(kaddr);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ts(tbase + kColS0 + 128 * sb, tbase + kColQ + 8 * kk,
+                         desc_plus(kd, kmajor16_off(kk)), kIdS, kk > 0);
+            mma_commit(bar(L::kSFull + sb));
+          }
+          if (j > 0) {
+            // dS_{j-1} is ready (and, for the unit's first dQ, dQ is free)
+            aborted = named_bar_or(kBarRelay, 64, aborted);
+            if (!aborted && lane == 0) {
+              tc_fence_after();
+              issue_dq(prev_kaddr, prev_sb, j > 1 ? 1u : 0u);
+              mma_commit(bar(L::kKEmpty + prev_ks));
+            }
+          }
+          // V_j has landed and S_j has been read: dP_j = dO_i V_j^T into sb
+          const uint32_t vs = v_it % L::kVSlots;
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+          if (!aborted && lane == 0) {
+            tc_fence_after();
+            const uint64_t vd = kmajor_base(sbase + L::kV0 + vs * kTile);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ts(tbase + kColS0 + 128 * sb, tbase + kColDO + 8 * kk,
+                         desc_plus(vd, kmajor16_off(kk)), kIdS, kk > 0);
+            mma_commit(bar(L::kDpFull));
+            mma_commit(bar(L::kVEmpty + vs));
+          }
           prev_kaddr = kaddr;
           prev_ks = ks;
+          prev_sb = sb;
           ++k_it;
           ++v_it;
           ++step_it;
         }
-        if (!ok) break;
         // dQ += dS_last K_last, then hand dQ to the warpgroups
-        ok = mbar_wait(bar(L::kDsReady), (step_it - 1) & 1, wd, 49);
-        if (!ok) break;
-        if (w.nsteps == 1 && unit_it > 0) {
-          ok = mbar_wait(bar(L::kDqFree), (unit_it - 1) & 1, wd, 50);
-          if (!ok) break;
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if (!aborted && lane == 0) {
+          tc_fence_after();
+          issue_dq(prev_kaddr, prev_sb, w.nsteps > 1 ? 1u : 0u);
+          mma_commit(bar(L::kKEmpty + prev_ks));
+          mma_commit(bar(L::kDqFull));
         }
-        tc_fence_after();
-        issue_dq(prev_kaddr, w.nsteps > 1 ? 1u : 0u);
-        mma_commit(bar(L::kKEmpty + prev_ks));
-        mma_commit(bar(L::kDqFull));
-        ++unit_it;
       }
-      mma_commit(bar(L::kDrain));
-      Watchdog dw = wd;
-      volatile int never = 0;
-      dw.abort_flag = &never;
-      dw.limit_ns = drain_limit_ns(wd.limit_ns);
-      mbar_wait(bar(L::kDrain), 0, dw, 51);
+      if (lane == 0) {
+        mma_commit(bar(L::kDrain));
+        Watchdog dw = wd;
+        volatile int never = 0;
+        dw.abort_flag = &never;
+        dw.limit_ns = drain_limit_ns(wd.limit_ns);
+        mbar_wait(bar(L::kDrain), 0, dw, 51);
+      }
     }
     __syncwarp();
+  } else if (warp == kWarpRelay) {
+    // ------------------------------------------------------------------ relay ---
+    // Walks the issuer's schedule: before each rendezvous, waits (all lanes)
+    // for what the next MMA group reads.  After an abort the waits are
+    // skipped but every rendezvous is still met.
+    uint32_t k_it = 0, v_it = 0, step_it = 0, unit_it = 0;
+    bool aborted = false;
+    auto wait_all = [&](uint32_t b, uint32_t par, int site) {
+      if (!aborted) aborted = !__all_sync(0xffffffffu, mbar_wait(b, par, wd, site));
+    };
+    for (int k = 0;; ++k) {
+      const int u = snake_unit(k, cta, G);
+      if (u >= num_units) break;
+      const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
+      if (w.nsteps == 0) continue;
+      for (int j = 0; j < w.nsteps; ++j) {
+        if (j == 0) wait_all(bar(L::kQFull), unit_it & 1, 45);
+        wait_all(bar(L::kKFull + k_it % L::kKSlots), (k_it / L::kKSlots) & 1, 46);
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if (j > 0) {
+          wait_all(bar(L::kDsReady), (step_it - 1) & 1, 47);
+          if (j == 1 && unit_it > 0) wait_all(bar(L::kDqFree), (unit_it - 1) & 1, 48);
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+        }
+        wait_all(bar(L::kVFull + v_it % L::kVSlots), (v_it / L::kVSlots) & 1, 55);
+        wait_all(bar(L::kSRead), step_it & 1, 56);
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        ++k_it;
+        ++v_it;
+        ++step_it;
+      }
+      wait_all(bar(L::kDsReady), (step_it - 1) & 1, 49);
+      if (w.nsteps == 1 && unit_it > 0) wait_all(bar(L::kDqFree), (unit_it - 1) & 1, 50);
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      ++unit_it;
+    }
   } else {
     // ------------------------------------------------------ compute warpgroups ---
     const int h = warp >> 2;                 // key half of every step
     const int r = threadIdx.x & 127;         // TMEM lane: query row
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t dp_addr = tbase + lane_base + kColDP2 + 64 * h;
     const uint32_t dq_addr = tbase + lane_base + kColDQ + 64 * h;
     const float sl2 = p.scale_log2;
     uint32_t unit_it = 0, step_it = 0;
@@ -838,9 +894,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const bool diag = CAUSAL && (j == w.i);
+        // S_j, then dP_j and dS_j, in this step's buffer
         const uint32_t s_addr = tbase + lane_base + kColS0 + 128 * sb + 64 * h;
+        const uint32_t dp_addr = s_addr;
         // ---- P = exp2(S c - LSE log2 e), kept in fp32 for dS.  Both
-        // 32-column chunks are loaded before one wait.
+        // 32-column chunks are loaded before one wait; then the buffer may
+        // take dP_j.
         float pr[64];
         {
           uint32_t sa[32], sc[32];
@@ -849,6 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           reg_fence32(sa);
           reg_fence32(sc);
+          tc_fence_before();
+          mbar_arrive(bar(L::kSRead));
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const uint32_t* src = e < 16 ? sa : sc;
@@ -977,25 +1038,26 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 }
 
 template <typename Kern>
-cudaError_t launch_persistent(Kern kern, int bytes, bool* configured, const BwdLaunch& a,
-                              int units) {
+cudaError_t launch_persistent(Kern kern, int threads, int bytes, bool* configured,
+                              const BwdLaunch& a, int units) {
   if (!*configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     *configured = true;
   }
   const int grid = units < a.num_sms ? units : a.num_sms;
-  kern<<<grid, kThreads, bytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, a.params);
+  kern<<<grid, threads, bytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, a.params);
   return cudaGetLastError();
 }
 
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_main(const BwdLaunch& a) {
   static bool dkv_configured = false, dq_configured = false;
-  cudaError_t e = launch_persistent(bwd_dkv_kernel<CAUSAL, BF16>, DkvLayout::kBytes,
+  cudaError_t e = launch_persistent(bwd_dkv_kernel<CAUSAL, BF16>, kThreads, DkvLayout::kBytes,
                                     &dkv_configured, a, a.params.BHkv * a.params.n_kblocks);
   if (e != cudaSuccess) return e;
-  return launch_persistent(bwd_dq_kernel<CAUSAL, BF16>, DqLayout::kBytes, &dq_configured, a,
+  return launch_persistent(bwd_dq_kernel<CAUSAL, BF16>, kThreadsDq, DqLayout::kBytes,
+                           &dq_configured, a,
                            a.params.BH * a.params.n_qtiles);
 }
 

@@ -260,6 +260,15 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 
 // Arrive (once) on an mbarrier when all previously issued tcgen05 async
 // operations of this thread have completed.
+// Asynchronous copy of a 128-row x 32-byte matrix from shared memory (matrix
+// descriptor, same format as an MMA operand) into tensor memory: row r lands
+// in lane r, columns [taddr, taddr + 8).  Runs in the tensor pipe in issue
+// order with the MMAs of the same thread.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
