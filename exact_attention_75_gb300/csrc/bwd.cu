@@ -24,13 +24,13 @@
 // accumulator in tensor memory; P and dS feed the dV / dK / dQ products
 // from tensor memory.
 //
-// CTA organisation (bwd_dkv 320 threads, bwd_dq 352):
+// CTA organisation of both kernels (352 threads):
 //   warps 0-3 / 4-7  compute warpgroups, one per half of the 128 columns of
 //                    S (query columns in bwd_dkv, key columns in bwd_dq);
 //                    thread = TMEM lane = row
 //   warp 8           TMA producer
 //   warp 9           tcgen05 issuer + tensor-memory owner
-//   warp 10          (bwd_dq) relay: waits on the pipeline's mbarriers and
+//   warp 10          relay: waits on the pipeline's mbarriers and
 //                    meets the issuer at a named barrier, so that the issuer
 //                    never touches shared memory between its commits
 #include <cuda.h>
@@ -46,8 +46,7 @@ namespace attn {
 
 namespace {
 
-constexpr int kThreads = 320;    // bwd_dkv
-constexpr int kThreadsDq = 352;  // bwd_dq (+ relay warp)
+constexpr int kThreads = 352;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpRelay = 10;
@@ -305,12 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ tcgen05 issuer ---
     // Per step s: S^T(s) | dK(s-1) | dP^T(s) | dV(s); after the unit's last
-    // step its dK.
-    if (lane == 0) {
+    // step its dK.  Each group is issued after a rendezvous with the relay
+    // warp, which has seen its inputs complete; after an abort both warps
+    // still walk the whole schedule (issuing nothing), so every rendezvous
+    // pairs up.
+    {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_f16(128, 128, BF16, false, true);  // dV, dK
-      uint32_t kv_it = 0, st_it = 0, unit_it = 0;
-      bool ok = true;
+      uint32_t st_it = 0;
+      bool aborted = false;
       // K and V as K-major A operands of S^T / dP^T.
       const uint64_t kd_k = kmajor_base(sbase + L::kK), vd_k = kmajor_base(sbase + L::kV);
       // dK(s) += dS^T(s) Q_i(s) with Q from its ring slot; then the slots of
@@ -325,81 +327,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(L::kQEmpty + qs));
         mma_commit(bar(L::kDoEmpty + step % L::kDoSlots));
       };
-      for (int k = 0; ok; ++k) {
+      for (int k = 0;; ++k) {
         const int u = snake_unit(k, cta, G);
         if (u >= num_units) break;
         const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
-        ok = mbar_wait(bar(L::kKvFull), kv_it & 1, wd, 25);
-        if (!ok) break;
-        ++kv_it;
-        tc_fence_after();
-        for (int s = 0; s < w.nsteps && ok; ++s) {
+        for (int s = 0; s < w.nsteps; ++s) {
           const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
-          const uint32_t par = st_it & 1;
-          ok = mbar_wait(bar(L::kQFull + qs), (st_it / L::kQSlots) & 1, wd, 26);
-          if (!ok) break;
-          tc_fence_after();
+          // Q_i(s) (and at s = 0 the unit's K, V) have landed.
           // S^T = K Q_i^T (the previous P^T was consumed by the previous dV,
           // and its S^T read before that P^T was handed over)
-          const uint64_t qd = kmajor_base(sbase + L::kQ0 + qs * kTile);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + kColS, desc_plus(kd_k, kmajor16_off(kk)),
-                       desc_plus(qd, kmajor16_off(kk)), kIdS, kk > 0);
-          mma_commit(bar(L::kSFull));
-          // dK(s-1): its dS^T must be in tensor memory
-          if (s > 0) {
-            ok = mbar_wait(bar(L::kDsReady), par ^ 1, wd, 27);
-            if (!ok) break;
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+          if (!aborted && lane == 0) {
             tc_fence_after();
-            issue_dk(st_it - 1, s > 1 ? 1u : 0u);
+            const uint64_t qd = kmajor_base(sbase + L::kQ0 + qs * kTile);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ss(tbase + kColS, desc_plus(kd_k, kmajor16_off(kk)),
+                         desc_plus(qd, kmajor16_off(kk)), kIdS, kk > 0);
+            mma_commit(bar(L::kSFull));
           }
-          // dP^T = V dO_i^T (dS^T(s-1) in these columns has just been consumed)
-          ok = mbar_wait(bar(L::kDoFull + ds), (st_it / L::kDoSlots) & 1, wd, 28);
-          if (!ok) break;
-          tc_fence_after();
+          // dK(s-1): its dS^T is in tensor memory
+          if (s > 0) {
+            aborted = named_bar_or(kBarRelay, 64, aborted);
+            if (!aborted && lane == 0) {
+              tc_fence_after();
+              issue_dk(st_it - 1, s > 1 ? 1u : 0u);
+            }
+          }
+          // dP^T = V dO_i^T once dO_i has landed (dS^T(s-1) in these
+          // columns has just been consumed)
           const uint32_t doaddr = sbase + L::kDo0 + ds * kTile;
-          const uint64_t dod = kmajor_base(doaddr);
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+          if (!aborted && lane == 0) {
+            tc_fence_after();
+            const uint64_t dod = kmajor_base(doaddr);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tbase + kColDP, desc_plus(vd_k, kmajor16_off(kk)),
-                       desc_plus(dod, kmajor16_off(kk)), kIdS, kk > 0);
-          mma_commit(bar(L::kDpFull));
-          // dV / dK of the previous unit have been stored
-          if (s == 0 && unit_it > 0) {
-            ok = mbar_wait(bar(L::kDkvFree), (unit_it - 1) & 1, wd, 29);
-            if (!ok) break;
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ss(tbase + kColDP, desc_plus(vd_k, kmajor16_off(kk)),
+                         desc_plus(dod, kmajor16_off(kk)), kIdS, kk > 0);
+            mma_commit(bar(L::kDpFull));
           }
-          // dV += P^T dO_i  (A = P^T from tensor memory)
-          ok = mbar_wait(bar(L::kPReady), par, wd, 30);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dod_mn = mnmajor_base(doaddr);
+          // dV += P^T dO_i (A = P^T from tensor memory) once P^T is there
+          // (and, at s = 0, the previous unit's dV / dK have been stored)
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+          if (!aborted && lane == 0) {
+            tc_fence_after();
+            const uint64_t dod_mn = mnmajor_base(doaddr);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ts(tbase + kColDV, tbase + kColS + half_packed_col(kk),
-                       desc_plus(dod_mn, mnmajor16_off(kk)), kIdKV, kk > 0 || s > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ts(tbase + kColDV, tbase + kColS + half_packed_col(kk),
+                         desc_plus(dod_mn, mnmajor16_off(kk)), kIdKV, kk > 0 || s > 0 ? 1u : 0u);
+          }
           ++st_it;
         }
-        if (!ok) break;
         // the unit's last dK, then hand dK / dV to the warpgroups
-        ok = mbar_wait(bar(L::kDsReady), (st_it - 1) & 1, wd, 31);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dk(st_it - 1, w.nsteps > 1 ? 1u : 0u);
-        mma_commit(bar(L::kDkvFull));
-        mma_commit(bar(L::kKvEmpty));
-        ++unit_it;
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if (!aborted && lane == 0) {
+          tc_fence_after();
+          issue_dk(st_it - 1, w.nsteps > 1 ? 1u : 0u);
+          mma_commit(bar(L::kDkvFull));
+          mma_commit(bar(L::kKvEmpty));
+        }
       }
-      mma_commit(bar(L::kDrain));
-      Watchdog dw = wd;
-      volatile int never = 0;
-      dw.abort_flag = &never;
-      dw.limit_ns = drain_limit_ns(wd.limit_ns);
-      mbar_wait(bar(L::kDrain), 0, dw, 32);
+      if (lane == 0) {
+        mma_commit(bar(L::kDrain));
+        Watchdog dw = wd;
+        volatile int never = 0;
+        dw.abort_flag = &never;
+        dw.limit_ns = drain_limit_ns(wd.limit_ns);
+        mbar_wait(bar(L::kDrain), 0, dw, 32);
+      }
     }
     __syncwarp();
+  } else if (warp == kWarpRelay) {
+    // ------------------------------------------------------------------ relay ---
+    // Walks the issuer's schedule: before each rendezvous, waits (all lanes)
+    // for what the next MMA group reads.  After an abort the waits are
+    // skipped but every rendezvous is still met.
+    uint32_t kv_it = 0, st_it = 0, unit_it = 0;
+    bool aborted = false;
+    auto wait_all = [&](uint32_t b, uint32_t par, int site) {
+      if (!aborted) aborted = !__all_sync(0xffffffffu, mbar_wait(b, par, wd, site));
+    };
+    for (int k = 0;; ++k) {
+      const int u = snake_unit(k, cta, G);
+      if (u >= num_units) break;
+      const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
+      if (w.nsteps == 0) continue;
+      wait_all(bar(L::kKvFull), kv_it & 1, 25);
+      ++kv_it;
+      for (int s = 0; s < w.nsteps; ++s) {
+        const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
+        const uint32_t par = st_it & 1;
+        wait_all(bar(L::kQFull + qs), (st_it / L::kQSlots) & 1, 26);
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if (s > 0) {
+          wait_all(bar(L::kDsReady), par ^ 1, 27);
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+        }
+        wait_all(bar(L::kDoFull + ds), (st_it / L::kDoSlots) & 1, 28);
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if (s == 0 && unit_it > 0) wait_all(bar(L::kDkvFree), (unit_it - 1) & 1, 29);
+        wait_all(bar(L::kPReady), par, 30);
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        ++st_it;
+      }
+      wait_all(bar(L::kDsReady), (st_it - 1) & 1, 31);
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      ++unit_it;
+    }
   } else {
     // ------------------------------------------------------ compute warpgroups ---
     const int h = warp >> 2;                 // query half of every step
@@ -621,7 +658,7 @@ __device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
 }
 
 template <bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(kThreadsDq, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdParams p) {
@@ -1056,7 +1093,7 @@ cudaError_t launch_main(const BwdLaunch& a) {
   cudaError_t e = launch_persistent(bwd_dkv_kernel<CAUSAL, BF16>, kThreads, DkvLayout::kBytes,
                                     &dkv_configured, a, a.params.BHkv * a.params.n_kblocks);
   if (e != cudaSuccess) return e;
-  return launch_persistent(bwd_dq_kernel<CAUSAL, BF16>, kThreadsDq, DqLayout::kBytes,
+  return launch_persistent(bwd_dq_kernel<CAUSAL, BF16>, kThreads, DqLayout::kBytes,
                            &dq_configured, a,
                            a.params.BH * a.params.n_qtiles);
 }
