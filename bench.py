@@ -173,11 +173,14 @@ def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
 class Step:
     """All buffers of one step, resident on the device."""
 
-    def __init__(self, attn, w: wl.Workload, dev, components):
+    def __init__(self, attn, w: wl.Workload, dev, components, like=None):
         self.attn, self.w, self.dev, self.components = attn, w, dev, components
-        inp = wl.make_inputs(w, with_do=True)
-        self.host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
-        self.signs = inp["signs"].to(dev)
+        if like is None:
+            inp = wl.make_inputs(w, with_do=True)
+            self.host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+            self.signs = inp["signs"].to(dev)
+        else:  # a second set of device buffers on the same pinned host inputs
+            self.host, self.signs = like.host, like.signs
         self.q, self.k, self.v, self.do = (self.host[n].to(dev) for n in ("q", "k", "v", "do"))
         B, H, N, d = w.B, w.H, w.N, w.d
         self.o = torch.empty_like(self.q)
@@ -422,28 +425,59 @@ def run_gpu(args, rank, world, local_rank):
     if status[0] != 0:
         raise RuntimeError(f"device status after timed region: {status}")
 
-    # e2e through the public API with host buffers: H2D of the inputs and
-    # D2H of every output inside the timed region.
-    outs = st.outputs()
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    # e2e through the public API with host buffers: every step copies its
+    # inputs from pinned host memory and every output back, inside the timed
+    # region.  Steps are pipelined over two sets of device buffers: the H2D
+    # copy of step k+1 (one copy stream) and the D2H copy of step k (another)
+    # run while step k computes.
+    sets = [st, Step(attn, rank_workload(w, rank), dev, comps, like=st)]
+    outs = [x.outputs() for x in sets]
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs[0]]
     h2d = sum(st.host[n].numel() * st.host[n].element_size() for n in ("q", "k", "v", "do"))
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    d2h = sum(o.numel() * o.element_size() for o in outs[0])
     e2e_steps = max(3, min(args.steps, 20))
-    for it in range(e2e_steps + 1):
-        if it == 1:
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        for n in ("q", "k", "v", "do"):
-            getattr(st, n).copy_(st.host[n], non_blocking=True)
-        for c in comps:
-            st.run(c)
-        for o, h in zip(outs, host_out):
-            h.copy_(o, non_blocking=True)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def e2e_round(nsteps, start):
+        ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
+        up.wait_event(start)
+        down.wait_event(start)
+        for k in range(nsteps):
+            b = k % 2
+            x = sets[b]
+            with torch.cuda.stream(up):
+                if k >= 2:
+                    up.wait_event(ev["comp"][b])  # step k-2 has read these inputs
+                for n in ("q", "k", "v", "do"):
+                    getattr(x, n).copy_(x.host[n], non_blocking=True)
+                ev["in"][b].record(up)
+            stream.wait_event(ev["in"][b])
+            if k >= 2:
+                stream.wait_event(ev["out"][b])  # step k-2's outputs are on the host
+            for c in comps:
+                x.run(c)
+            ev["comp"][b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(ev["comp"][b])
+                for o, h in zip(outs[b], host_out):
+                    h.copy_(o, non_blocking=True)
+                ev["out"][b].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+
+    torch.cuda.synchronize()
+    warm = torch.cuda.Event()
+    warm.record(stream)
+    e2e_round(2, warm)  # untimed
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    e2e_round(e2e_steps, e0)
     e1 = torch.cuda.Event(enable_timing=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    del sets[1]
 
     split = split_kv_timing(attn, st, w, stream, n_split=SPLIT_KV_N)
     gqa = gqa_timing(attn, st, w, stream, GQA_KV_HEADS) if "bwd" in comps else None
@@ -575,7 +609,10 @@ def main():
             "breakdown": breakdown, "roofline": roof, "clocks": r["clocks"],
             "gpu_launches": r["launches"],
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}}
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                    "note": "public API, pinned host buffers; each step's H2D and D2H copies "
+                            "overlap the neighbouring steps' compute (two device buffer "
+                            "sets, two copy streams)"}}
     if r.get("split"):
         sp = dict(r["split"])
         mb = sp.pop("merge_bytes")
