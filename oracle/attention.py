@@ -46,6 +46,7 @@ import numpy as np
 __all__ = [
     "scores", "allowed_mask", "masked_softmax", "attention_head", "attention",
     "attention_rows", "online_softmax_attention_head", "attention_backward_head",
+    "attention_backward_dq_rows",
     "attention_backward", "E4M3_MAX", "e4m3_decode", "e4m3_encode", "hadamard_matrix",
     "rotation_matrix", "quantize_blocks", "dequantize_blocks", "rmse",
     "split_key_ranges", "attention_partial_head", "attention_split", "merge_partials",
@@ -401,6 +402,32 @@ def attention_backward_head(q, k, v, do, causal: bool, scale: float):
     dQ = scale * (dS @ k)
     dK = scale * (dS.T @ q)
     return dQ, dK, dV, dS
+
+
+def attention_backward_dq_rows(q, k, v, do, rows: Sequence[int], causal: bool, scale: float):
+    """dQ of selected query rows of one head (q, k, v, do: [N, d]).
+
+    Row i of dQ needs only row i of P: P_i = softmax(scale q_i K^T, masked),
+    O_i = P_i V, D_i = dO_i . O_i, dP_i = dO_i V^T, dS_i = P_i o (dP_i - D_i),
+    dQ_i = scale dS_i K (the formulas of attention_backward_head restricted
+    to one row), so long sequences can be checked on sampled rows.
+    Pinned against attention_backward_head in tests/test_oracle.py.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    rows = np.asarray(rows, dtype=np.int64)
+    S = scale * (q[rows] @ k.T)
+    allowed = np.ones_like(S, dtype=bool)
+    if causal:
+        allowed = np.arange(k.shape[0])[None, :] <= rows[:, None]
+    P, _ = masked_softmax(S, allowed)
+    O = P @ v
+    D = np.sum(do[rows] * O, axis=1, keepdims=True)
+    dP = do[rows] @ v.T
+    dS = P * (dP - D)
+    return scale * (dS @ k)
 
 
 def attention_backward(q, k, v, do, causal: bool, scale: float, heads=None):

@@ -584,3 +584,15 @@ def test_varlen_gradient_by_finite_differences():
         vp[g, i, c] += eps
         vm[g, i, c] -= eps
         assert abs((loss(q, k, vp) - loss(q, k, vm)) / (2 * eps) - dV[g, i, c]) < 1e-7
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dq_rows_equal_the_full_backward(causal):
+    """The row-restricted dQ (for sampled rows of long sequences) equals the
+    full-matrix backward, itself pinned by finite differences."""
+    rng = np.random.default_rng(12 + causal)
+    q, k, v, do = (rng.standard_normal((37, 5)) for _ in range(4))
+    dQ, _, _, _ = oracle.attention_backward_head(q, k, v, do, causal, 0.45)
+    rows = [0, 1, 17, 36]
+    assert np.allclose(oracle.attention_backward_dq_rows(q, k, v, do, rows, causal, 0.45),
+                       dQ[rows], rtol=0, atol=1e-13)
