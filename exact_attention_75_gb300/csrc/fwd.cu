@@ -481,31 +481,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
         float s[128];
-        float g0 = 1.f, g1 = 1.f;
+        // E4M3: keys [0,64) and [64,128) of the block have their own K and V
+        // scales; the raw scores are scaled inside the exponent argument
+        // (f0 / f1 include the Q scale and scale * log2 e) and the row max is
+        // taken per half on the raw scores (scaling by f > 0 keeps the order).
+        float g0 = 1.f, g1 = 1.f, f0 = 1.f, f1 = 1.f;
         if constexpr (FP8) {
-          // keys [0,64) and [64,128) of the block have their own K and V scales
           const int b0 = 2 * (w.kb0 + j), b1 = min(b0 + 1, p.n_sblocks - 1);
-          const float f0 = fq * ksc[b0];
-          const float f1 = fq * ksc[b1];
+          f0 = fq * ksc[b0];
+          f1 = fq * ksc[b1];
           g0 = vsc[b0] / sv_max;
           g1 = vsc[b1] / sv_max;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float2 f = c < 2 ? make_float2(f0, f0) : make_float2(f1, f1);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 v = __fmul2_rn(
-                  make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), f);
-              s[c * 32 + 2 * i] = v.x;
-              s[c * 32 + 2 * i + 1] = v.y;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
         }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
         const int jk = w.kb0 + j;  // key block index
         const bool diag = CAUSAL && (jk == tile);
         const bool tail = (jk == w.nkb - 1) && (w.len & 127);
@@ -515,8 +506,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
-        const float mx = row_max128(s);
-        const float m_blk = FP8 ? mx : mx * sl2;
+        float m_blk;
+        if constexpr (FP8) {
+          float h0 = fmax3(s[0], s[1], s[2]), h1 = fmax3(s[64], s[65], s[66]);
+          float h2 = fmax3(s[3], s[4], s[5]), h3 = fmax3(s[67], s[68], s[69]);
+#pragma unroll
+          for (int c = 6; c < 62; c += 4) {
+            h0 = fmax3(h0, s[c], s[c + 1]);
+            h2 = fmax3(h2, s[c + 2], s[c + 3]);
+            h1 = fmax3(h1, s[64 + c], s[64 + c + 1]);
+            h3 = fmax3(h3, s[64 + c + 2], s[64 + c + 3]);
+          }
+          h0 = fmax3(h0, h2, fmaxf(s[62], s[63]));
+          h1 = fmax3(h1, h3, fmaxf(s[126], s[127]));
+          m_blk = fmaxf(h0 * f0, h1 * f1);
+        } else {
+          m_blk = row_max128(s) * sl2;
+        }
         if (j == 0) {
           m = m_blk;
         } else {
@@ -555,11 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 2; ++c) {
             const float2 g2 = c == 0 ? make_float2(g0, g0) : make_float2(g1, g1);
             uint32_t pk[16];
+            const float2 fc2 = c == 0 ? make_float2(f0, f0) : make_float2(f1, f1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int col = c * 64 + 4 * i;
-              const float2 x01 = __fadd2_rn(make_float2(s[col], s[col + 1]), nm2);
-              const float2 x23 = __fadd2_rn(make_float2(s[col + 2], s[col + 3]), nm2);
+              const float2 x01 = __ffma2_rn(make_float2(s[col], s[col + 1]), fc2, nm2);
+              const float2 x23 = __ffma2_rn(make_float2(s[col + 2], s[col + 3]), fc2, nm2);
               float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
               float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
               rs2[(2 * i) & 3] = __fadd2_rn(rs2[(2 * i) & 3], p01);
