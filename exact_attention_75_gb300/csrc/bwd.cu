@@ -22,7 +22,9 @@
 // taken by an N = 128 MMA with both operands in shared memory) is what
 // bounds these kernels.  Every MMA here has N = 128 and keeps its
 // accumulator in tensor memory; P and dS feed the dV / dK / dQ products
-// from tensor memory.
+// from tensor memory, and in bwd_dq Q_i and dO_i are copied into tensor
+// memory once per query tile so that S and dP read only K_j / V_j from
+// shared memory.
 //
 // CTA organisation of both kernels (352 threads):
 //   warps 0-3 / 4-7  compute warpgroups, one per half of the 128 columns of
