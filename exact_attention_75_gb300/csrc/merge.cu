@@ -5,11 +5,14 @@
 // (O_s, LSE_s):
 //   m = max_s LSE_s,  l = sum_s exp(LSE_s - m),
 //   LSE = m + log l,  O = sum_s exp(LSE_s - m) O_s / l.
-// Splits whose LSE is -inf (no visible key) are skipped without reading their
-// O; a row with no key at all gets O = 0 and LSE = -inf.
+// Splits whose LSE is -inf (no visible key) contribute nothing (their O is
+// ignored, selected away rather than multiplied by zero); a row with no key
+// at all gets O = 0 and LSE = -inf.
 //
-// One warp per row (d/32 values per lane, so each split's row is one
-// coalesced 2*d-byte read), grid-stride over rows; arithmetic in fp32.
+// d/8 lanes per row (8 values, one 16-byte read of each split's row per
+// lane), so a warp merges 32/(d/8) rows at once; the splits' rows are read
+// four at a time so their loads are in flight together; grid-stride over
+// rows; arithmetic in fp32.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -21,65 +24,78 @@ namespace attn {
 
 namespace {
 
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
+  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (BF16) {
+      x[2 * i] = __uint_as_float(wd[i] << 16);
+      x[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+    } else {
+      x[2 * i] = __half2float(__ushort_as_half((unsigned short)(wd[i] & 0xFFFFu)));
+      x[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(wd[i] >> 16)));
+    }
+  }
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__ o_part,
                                                     const float* __restrict__ lse_part,
                                                     int n_split, long rows,
                                                     uint16_t* __restrict__ o,
                                                     float* __restrict__ lse) {
-  constexpr int E = D / 32;  // values per lane: 4 (d = 128) or 2 (d = 64)
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  constexpr int kBatch = 4;  // splits whose rows are read together
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanesPerRow;  // row of the warp
+  const int col = (lane % kLanesPerRow) * 8;
   const long warp0 = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  for (long row = warp0; row < rows; row += nwarps) {
+  for (long row0 = warp0 * kRowsPerWarp; row0 < rows; row0 += nwarps * kRowsPerWarp) {
+    const long row = row0 + sub;
+    const bool live = row < rows;
+    const long rrow = live ? row : rows - 1;  // in-range address for idle lanes
     float m = -INFINITY;
-    for (int s = 0; s < n_split; ++s) m = fmaxf(m, lse_part[(size_t)s * rows + row]);
-    float acc[E];
+    for (int s = 0; s < n_split; ++s) m = fmaxf(m, lse_part[(size_t)s * rows + rrow]);
+    float acc[8];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     float l = 0.f;
     if (m != -INFINITY) {
-      for (int s = 0; s < n_split; ++s) {
-        const float ls = lse_part[(size_t)s * rows + row];
-        if (ls == -INFINITY) continue;  // warp-uniform
-        const float w = expf(ls - m);
-        l += w;
-        const uint16_t* src = o_part + ((size_t)s * rows + row) * D + lane * E;
-        uint32_t word[E / 2];
-        if constexpr (E == 4) {
-          const uint2 t = *reinterpret_cast<const uint2*>(src);
-          word[0] = t.x;
-          word[1] = t.y;
-        } else {
-          word[0] = *reinterpret_cast<const uint32_t*>(src);
+      for (int s0 = 0; s0 < n_split; s0 += kBatch) {
+        uint4 w[kBatch];
+        float ls[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int sk = min(s0 + k, n_split - 1);
+          ls[k] = s0 + k < n_split ? lse_part[(size_t)sk * rows + rrow] : -INFINITY;
+          w[k] = *reinterpret_cast<const uint4*>(o_part + ((size_t)sk * rows + rrow) * D + col);
         }
 #pragma unroll
-        for (int e = 0; e < E / 2; ++e) {
-          float lo, hi;
-          if (BF16) {
-            lo = __uint_as_float(word[e] << 16);
-            hi = __uint_as_float(word[e] & 0xFFFF0000u);
-          } else {
-            lo = __half2float(__ushort_as_half((unsigned short)(word[e] & 0xFFFFu)));
-            hi = __half2float(__ushort_as_half((unsigned short)(word[e] >> 16)));
-          }
-          acc[2 * e] = fmaf(w, lo, acc[2 * e]);
-          acc[2 * e + 1] = fmaf(w, hi, acc[2 * e + 1]);
+        for (int k = 0; k < kBatch; ++k) {
+          const bool use = ls[k] != -INFINITY;
+          const float wt = use ? expf(ls[k] - m) : 0.f;
+          l += wt;
+          float x[8];
+          unpack8<BF16>(w[k], x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = use ? fmaf(wt, x[e], acc[e]) : acc[e];
         }
       }
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint32_t packed[E / 2];
+    uint32_t packed[4];
 #pragma unroll
-    for (int e = 0; e < E / 2; ++e)
+    for (int e = 0; e < 4; ++e)
       packed[e] = BF16 ? pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv)
                        : pack_f16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-    uint16_t* dst = o + (size_t)row * D + lane * E;
-    if constexpr (E == 4)
-      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-    else
-      *reinterpret_cast<uint32_t*>(dst) = packed[0];
-    if (lane == 0) lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
+    if (live) {
+      *reinterpret_cast<uint4*>(o + (size_t)row * D + col) =
+          make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      if (col == 0) lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
+    }
   }
 }
 
