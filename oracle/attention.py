@@ -28,7 +28,7 @@ What this file computes, and how each function is pinned to something other
 than itself, is listed per function.  All floating point is fp64 unless a
 function is explicitly about the fp32/E4M3 encodings.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * LSE is the natural log of the sum of exp of the *scaled* scores.
 * Causal masking is top-left aligned: key j is visible to query i iff j <= i.
@@ -135,8 +135,8 @@ def attention_rows(q, k, v, rows: Sequence[int], causal: bool, scale: float):
 # attention over a subset of the keys and a way to combine such partial
 # results; the "Insights" of [FA2-review] note that the log-sum-exp is all
 # that has to be kept besides O.  The pages give no formula; the one below is
-# the plain consequence of the softmax definition (a reading, listed in
-# the design doc): over disjoint key sets K_s with partial results
+# the plain consequence of the softmax definition (a reading): over
+# disjoint key sets K_s with partial results
 # O_s = sum_{j in K_s} exp(S_ij - LSE_s) v_j and LSE_s = log sum_{j in K_s}
 # exp(S_ij), the result over their union is
 #   LSE = log sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
@@ -215,8 +215,8 @@ def merge_partials(O_parts, LSE_parts):
 # ---------------------------------------------------------------------------
 #
 # The "Insights" of [FA2-review] link GQA ("Training Generalized Multi-Query
-# Transformer Models") without spelling it out.  Reading (listed in
-# the design doc): with Hq query heads and Hkv key/value heads, Hkv dividing Hq and
+# Transformer Models") without spelling it out.  Reading: with Hq query
+# heads and Hkv key/value heads, Hkv dividing Hq and
 # G = Hq / Hkv, query head h attends with key/value head h // G (contiguous
 # groups; Hkv = 1 is multi-query attention).  Each query head's attention is
 # the plain definition; the gradient of a shared key/value head is the sum of
