@@ -251,7 +251,7 @@ def component_bytes(w: wl.Workload):
 
 
 def available_components(attn, step_probe=None):
-    """Components whose entry points are implemented in this build."""
+    """Components to run (all by default; ATTN_BENCH_COMPONENTS selects a subset)."""
     return [c for c in COMPONENTS if c in os.environ.get("ATTN_BENCH_COMPONENTS",
                                                            ",".join(COMPONENTS)).split(",")]
 
