@@ -251,9 +251,8 @@ def component_bytes(w: wl.Workload):
 
 
 def available_components(attn, step_probe=None):
-    """Components to run (all by default; ATTN_BENCH_COMPONENTS selects a subset)."""
-    return [c for c in COMPONENTS if c in os.environ.get("ATTN_BENCH_COMPONENTS",
-                                                           ",".join(COMPONENTS)).split(",")]
+    """The components of one step (every one is always run)."""
+    return list(COMPONENTS)
 
 
 SPLIT_KV_N = 4  # key splits of the split-KV measurement
