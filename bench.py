@@ -540,8 +540,8 @@ def main():
         if rank != 0:
             return
         per_step = []
-        for _ in range(args.warmup > 0 and 1 or 0):
-            cpu_oracle_sample(budget_s=4.0)
+        for _ in range(args.warmup):  # untimed warm-up samples
+            cpu_oracle_sample(budget_s=1.0)
         heads_total, t_total = 0, 0.0
         for _ in range(args.steps):
             tf, dt, heads, cores = cpu_oracle_sample(budget_s=min(20.0, 120.0 / args.steps))
