@@ -339,7 +339,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(varlen ? 1 : B, H, N, d))
     return ATTN_ERR_INVALID_ARG;
@@ -390,6 +390,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   a.stream = static_cast<cudaStream_t>(stream);
   a.causal = causal != 0;
   a.bf16 = dtype == ATTN_BF16;
+  a.d = d;
   if (varlen) {
     cudaError_t e = launch_varlen_check(cu_seqlens, B, N, max_seqlen, di->status, a.stream);
     if (e != cudaSuccess) return launch_result(e);

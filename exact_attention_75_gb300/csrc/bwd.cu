@@ -55,7 +55,9 @@ constexpr int kWarpRelay = 10;
 constexpr uint32_t kBarRelay = 3;  // named barrier: relay warp + issuer warp (64 threads)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStatusLayout = 5;  // shared memory not 1024-byte aligned
-constexpr int kTile = 32768;           // 128 x 128 16-bit values
+// Bytes of a 128-row tile of 16-bit values with D columns.
+template <int D>
+constexpr int kTileBytes = 128 * D * 2;
 
 // Column of the K-step kk (16 values of the contraction index) of a 16-bit
 // operand that the two warpgroups wrote into the first 32 columns of their
@@ -68,11 +70,12 @@ __device__ __forceinline__ uint32_t pack16x2(bool bf16, float lo, float hi) {
   return bf16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
 
-// Loads a 128 x 128 16-bit tile (two 64-column boxes) with TMA.
+// Loads a 128 x D 16-bit tile (D/64 boxes of 64 columns) with TMA.
+template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                           int row0, int bh) {
-  tma_load_3d(dst, map, bar, 0, row0, bh);
-  tma_load_3d(dst + 16384, map, bar, 64, row0, bh);
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * 16384, map, bar, 64 * h, row0, bh);
 }
 
 // ============================================================ dK, dV kernel ===
@@ -82,7 +85,9 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
 // overlaps dV(s) and S^T(s+1).  Q_i is then read until the next step (by
 // dK), so Q has a ring of 3 slots; dO_i and the -LSE / -D vectors of its
 // queries have one of 2 slots.
+template <int D>
 struct DkvLayout {
+  static constexpr int kTile = kTileBytes<D>;
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
   static constexpr int kQSlots = 3, kDoSlots = 2;
@@ -166,12 +171,13 @@ __device__ __forceinline__ DkvUnit decode_dkv_unit(int u, const BwdParams& p) {
   return w;
 }
 
-template <bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                    const BwdParams p) {
-  using L = DkvLayout;
+  using L = DkvLayout<D>;
+  constexpr int kTile = L::kTile;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -240,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(L::kKvEmpty), (kv_it & 1) ^ 1, wd, 21);
         if (ok) {
           mbar_arrive_expect_tx(bar(L::kKvFull), 2 * kTile);
-          load_tile(sbase + L::kK, &tmK, bar(L::kKvFull), w.row0 + w.j * 128, w.zkv);
-          load_tile(sbase + L::kV, &tmV, bar(L::kKvFull), w.row0 + w.j * 128, w.zkv);
+          load_tile<D>(sbase + L::kK, &tmK, bar(L::kKvFull), w.row0 + w.j * 128, w.zkv);
+          load_tile<D>(sbase + L::kV, &tmV, bar(L::kKvFull), w.row0 + w.j * 128, w.zkv);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -255,14 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar(L::kQEmpty + qs), ((st_it / L::kQSlots) & 1) ^ 1, wd, 22);
           if (ok) {
             mbar_arrive_expect_tx(bar(L::kQFull + qs), kTile);
-            load_tile(sbase + L::kQ0 + qs * kTile, &tmQ, bar(L::kQFull + qs),
+            load_tile<D>(sbase + L::kQ0 + qs * kTile, &tmQ, bar(L::kQFull + qs),
                       w.row0 + i * 128, zq);
             ++q_issued;
             ok = mbar_wait(bar(L::kDoEmpty + ds), ((st_it / L::kDoSlots) & 1) ^ 1, wd, 23);
           }
           if (ok) {
             mbar_arrive_expect_tx(bar(L::kDoFull + ds), kTile);
-            load_tile(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds),
+            load_tile<D>(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds),
                       w.row0 + i * 128, zq);
             ++do_issued;
           }
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
-      constexpr uint32_t kIdKV = idesc_f16(128, 128, BF16, false, true);  // dV, dK
+      constexpr uint32_t kIdKV = idesc_f16(128, D, BF16, false, true);  // dV, dK
       uint32_t st_it = 0;
       bool aborted = false;
       // K and V as K-major A operands of S^T / dP^T.
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t qd = kmajor_base(sbase + L::kQ0 + qs * kTile);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < D / 16; ++kk)
               mma_f16_ss(tbase + kColS, desc_plus(kd_k, kmajor16_off(kk)),
                          desc_plus(qd, kmajor16_off(kk)), kIdS, kk > 0);
             mma_commit(bar(L::kSFull));
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t dod = kmajor_base(doaddr);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < D / 16; ++kk)
               mma_f16_ss(tbase + kColDP, desc_plus(vd_k, kmajor16_off(kk)),
                          desc_plus(dod, kmajor16_off(kk)), kIdS, kk > 0);
             mma_commit(bar(L::kDpFull));
@@ -564,9 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t src = tbase + lane_base + (h == 0 ? kColDV : kColDK);
       const float mult = (h == 0) ? 1.f : p.scale;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(h == 0 ? p.dv : p.dk) +
-                                            ((size_t)w.zkv * p.N + w.row0 + key) * 128);
+                                            ((size_t)w.zkv * p.N + w.row0 + key) * D);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t raw[32];
         tmem_ld32_sync(src + 32 * c, raw);
         uint32_t pk[16];
@@ -600,7 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // load has about two steps of MMA work to land in.  Q_i and dO_i land here
 // and are copied into tensor memory once per unit, so the S and dP MMAs read
 // only K_j / V_j from shared memory.
+template <int D>
 struct DqLayout {
+  static constexpr int kTile = kTileBytes<D>;
   static constexpr int kQ = 0;                    // Q_i staging (K-major)
   static constexpr int kDO = kTile;               // dO_i staging (K-major)
   static constexpr int kKSlots = 3, kVSlots = 2;
@@ -659,12 +667,13 @@ __device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
   return w;
 }
 
-template <bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdParams p) {
-  using L = DqLayout;
+  using L = DqLayout<D>;
+  constexpr int kTile = L::kTile;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {
@@ -730,22 +739,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(L::kQEmpty), (unit_it & 1) ^ 1, wd, 41);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kQFull), 2 * kTile);
-        load_tile(sbase + L::kQ, &tmQ, bar(L::kQFull), w.row0 + w.i * 128, w.zq);
-        load_tile(sbase + L::kDO, &tmDO, bar(L::kQFull), w.row0 + w.i * 128, w.zq);
+        load_tile<D>(sbase + L::kQ, &tmQ, bar(L::kQFull), w.row0 + w.i * 128, w.zq);
+        load_tile<D>(sbase + L::kDO, &tmDO, bar(L::kQFull), w.row0 + w.i * 128, w.zq);
         ++unit_it;
         for (int j = 0; j < w.nsteps && ok; ++j) {
           const uint32_t ks = k_it % L::kKSlots;
           ok = mbar_wait(bar(L::kKEmpty + ks), ((k_it / L::kKSlots) & 1) ^ 1, wd, 42);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kKFull + ks), kTile);
-          load_tile(sbase + L::kK0 + ks * kTile, &tmK, bar(L::kKFull + ks), w.row0 + j * 128,
+          load_tile<D>(sbase + L::kK0 + ks * kTile, &tmK, bar(L::kKFull + ks), w.row0 + j * 128,
                     w.zkv);
           ++k_it;
           const uint32_t vs = v_it % L::kVSlots;
           ok = mbar_wait(bar(L::kVEmpty + vs), ((v_it / L::kVSlots) & 1) ^ 1, wd, 43);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kVFull + vs), kTile);
-          load_tile(sbase + L::kV0 + vs * kTile, &tmV, bar(L::kVFull + vs), w.row0 + j * 128,
+          load_tile<D>(sbase + L::kV0 + vs * kTile, &tmV, bar(L::kVFull + vs), w.row0 + j * 128,
                     w.zkv);
           ++v_it;
         }
@@ -773,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nothing), so every rendezvous pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);  // S, dP
-      constexpr uint32_t kIdQ = idesc_f16(128, 128, BF16, false, true);   // dQ
+      constexpr uint32_t kIdQ = idesc_f16(128, D, BF16, false, true);     // dQ
       uint32_t k_it = 0, v_it = 0, step_it = 0;
       bool aborted = false;
       const uint64_t qd = kmajor_base(sbase + L::kQ), dod = kmajor_base(sbase + L::kDO);
@@ -804,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // previous unit's S and dP (their last readers) have completed:
               // the dS that the last dQ awaited was computed from them.
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
+              for (int kk = 0; kk < D / 16; ++kk) {
                 tmem_cp_128x256b(tbase + kColQ + 8 * kk, desc_plus(qd, kmajor16_off(kk)));
                 tmem_cp_128x256b(tbase + kColDO + 8 * kk, desc_plus(dod, kmajor16_off(kk)));
               }
@@ -814,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // were read by dQ_{j-2}, issued before).
             const uint64_t kd = kmajor_base(kaddr);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < D / 16; ++kk)
               mma_f16_ts(tbase + kColS0 + 128 * sb, tbase + kColQ + 8 * kk,
                          desc_plus(kd, kmajor16_off(kk)), kIdS, kk > 0);
             mma_commit(bar(L::kSFull + sb));
@@ -835,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t vd = kmajor_base(sbase + L::kV0 + vs * kTile);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < D / 16; ++kk)
               mma_f16_ts(tbase + kColS0 + 128 * sb, tbase + kColDO + 8 * kk,
                          desc_plus(vd, kmajor16_off(kk)), kIdS, kk > 0);
             mma_commit(bar(L::kDpFull));
@@ -908,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;                 // key half of every step
     const int r = threadIdx.x & 127;         // TMEM lane: query row
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t dq_addr = tbase + lane_base + kColDQ + 64 * h;
+    const uint32_t dq_addr = tbase + lane_base + kColDQ + (D / 2) * h;
     const float sl2 = p.scale_log2;
     uint32_t unit_it = 0, step_it = 0;
     bool ok = true;
@@ -1008,9 +1017,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++unit_it;
       tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * 128 + 64 * h);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D + (D / 2) * h);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t raw[32];
         tmem_ld32_sync(dq_addr + 32 * c, raw);
         uint32_t pk[16];
@@ -1039,22 +1048,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================================================ D kernel ===
 
-// D_i = sum_c dO_ic O_ic with one warp per row (4 values per lane, then a
+// D_i = sum_c dO_ic O_ic with one warp per row (D/32 values per lane, then a
 // butterfly of warp shuffles).
-template <bool BF16>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                      const uint16_t* __restrict__ dout,
                                                      float* __restrict__ delta, long rows) {
+  constexpr int W = D / 64;  // 32-bit words (two values each) per lane
   const long warp0 = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   for (long row = warp0; row < rows; row += nwarps) {
-    const uint2 a = reinterpret_cast<const uint2*>(o + row * 128)[lane];
-    const uint2 b = reinterpret_cast<const uint2*>(dout + row * 128)[lane];
+    uint32_t aw[W], bw[W];
+    if constexpr (W == 2) {
+      const uint2 a = reinterpret_cast<const uint2*>(o + row * D)[lane];
+      const uint2 b = reinterpret_cast<const uint2*>(dout + row * D)[lane];
+      aw[0] = a.x;
+      aw[1] = a.y;
+      bw[0] = b.x;
+      bw[1] = b.y;
+    } else {
+      aw[0] = reinterpret_cast<const uint32_t*>(o + row * D)[lane];
+      bw[0] = reinterpret_cast<const uint32_t*>(dout + row * D)[lane];
+    }
     float acc = 0.f;
-    const uint32_t aw[2] = {a.x, a.y}, bw[2] = {b.x, b.y};
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int e = 0; e < W; ++e) {
       float a0, a1, b0, b1;
       if (BF16) {
         a0 = __uint_as_float(aw[e] << 16);
@@ -1089,18 +1108,18 @@ cudaError_t launch_persistent(Kern kern, int threads, int bytes, bool* configure
   return cudaGetLastError();
 }
 
-template <bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_main(const BwdLaunch& a) {
   static bool dkv_configured = false, dq_configured = false;
-  cudaError_t e = launch_persistent(bwd_dkv_kernel<CAUSAL, BF16>, kThreads, DkvLayout::kBytes,
-                                    &dkv_configured, a, a.params.BHkv * a.params.n_kblocks);
+  cudaError_t e = launch_persistent(bwd_dkv_kernel<D, CAUSAL, BF16>, kThreads,
+                                    DkvLayout<D>::kBytes, &dkv_configured, a,
+                                    a.params.BHkv * a.params.n_kblocks);
   if (e != cudaSuccess) return e;
-  return launch_persistent(bwd_dq_kernel<CAUSAL, BF16>, kThreads, DqLayout::kBytes,
-                           &dq_configured, a,
-                           a.params.BH * a.params.n_qtiles);
+  return launch_persistent(bwd_dq_kernel<D, CAUSAL, BF16>, kThreads, DqLayout<D>::kBytes,
+                           &dq_configured, a, a.params.BH * a.params.n_qtiles);
 }
 
-template <bool BF16>
+template <int D, bool BF16>
 cudaError_t launch_all(const BwdLaunch& a) {
   const BwdParams& p = a.params;
   // rows of O / dO: every (batch, head) holds N, a packed variable-length
@@ -1109,17 +1128,18 @@ cudaError_t launch_all(const BwdLaunch& a) {
   long blocks = (rows + 7) / 8;
   const long cap = (long)a.num_sms * 16;
   if (blocks > cap) blocks = cap;
-  bwd_pre_kernel<BF16><<<(int)blocks, 256, 0, a.stream>>>(
+  bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, a.stream>>>(
       static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.delta, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return a.causal ? launch_main<true, BF16>(a) : launch_main<false, BF16>(a);
+  return a.causal ? launch_main<D, true, BF16>(a) : launch_main<D, false, BF16>(a);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const BwdLaunch& a) {
-  return a.bf16 ? launch_all<true>(a) : launch_all<false>(a);
+  if (a.d == 64) return a.bf16 ? launch_all<64, true>(a) : launch_all<64, false>(a);
+  return a.bf16 ? launch_all<128, true>(a) : launch_all<128, false>(a);
 }
 
 }  // namespace attn

@@ -21,7 +21,6 @@
 namespace {
 
 constexpr size_t kMaxRows = 4194304;  // B * H * N of one call
-constexpr int kHeadDim = 128;          // the only head dim of the backward kernels
 // The workspace attn_bwd expects: delta, fp32 per row (a multiple of 256 bytes).
 constexpr size_t kScratchBytes = kMaxRows * 4;
 
@@ -55,7 +54,7 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
                                         int causal, float scale, attn_dtype dtype,
                                         void* stream) {
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
-  if (d != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if ((size_t)B * (size_t)H * (size_t)N > kMaxRows) return ATTN_ERR_INVALID_ARG;
   void* scratch = nullptr;
   const attn_status st = scratch_address(&scratch);

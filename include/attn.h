@@ -136,8 +136,8 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *   workspace        : >= attn_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte
  *                      aligned, caller-owned; contents on entry are ignored
  *                      and on return are unspecified.
- * Only d = 128 is supported by the backward kernels (ATTN_ERR_UNSUPPORTED
- * otherwise).  dK, dV (per key tile) and dQ (per query tile) are each
+ * d in {64, 128} (ATTN_ERR_UNSUPPORTED otherwise).  dK, dV (per key tile)
+ * and dQ (per query tile) are each
  * accumulated in fp32 by one CTA in a fixed order, so the results are the
  * same from run to run.
  * Cite: FlashAttention-2 review, "Methods" (log-sum-exp kept for the backward
@@ -193,7 +193,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
  * dv [Hkv, total, d]; lse [Hq, total] from attn_fwd_varlen.  workspace: >=
  * attn_bwd_workspace_bytes(1, Hq, total, d) bytes, 256-byte aligned.  Rows of
  * dq, dk, dv outside every sequence (none when the offsets are valid) are
- * not written.  d = 128.  Offsets, checks and errors as in attn_fwd_varlen.
+ * not written.  d in {64, 128}.  Offsets, checks and errors as in
+ * attn_fwd_varlen.
  * Cite: as attn_bwd and attn_fwd_varlen.
  */
 attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
@@ -213,7 +214,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
  * same dQ, dK, dV as attn_bwd, with the same arguments minus the workspace;
  * the scratch (the fp32 delta vector) lives in a fixed device array inside
  * the library.
- *   Limit: B*H*N <= 4194304 query rows and d = 128; larger problems return
+ *   Limit: B*H*N <= 4194304 query rows and d in {64, 128}; larger problems return
  *   ATTN_ERR_INVALID_ARG, other head dims ATTN_ERR_UNSUPPORTED.
  *   Memory: the array (16 MB) is part of the library image and is held on
  *   every GPU that loads the library until the process exits.

@@ -47,12 +47,13 @@ def _check(w, grads, refs, heads=None):
         assert err <= REL_TOL, (w.name, name, err)
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 17), (1, 1, 128), (2, 1, 129),
                                    (1, 2, 300), (1, 1, 513), (2, 2, 1000)])
-def test_small_shapes_full(attn_lib, dtype, causal, B, H, N):
-    w = wl.Workload(f"bwd_{B}x{H}x{N}", "bwd", B, H, N, 128, dtype, causal, seed=7 + N)
+def test_small_shapes_full(attn_lib, dtype, causal, B, H, N, d):
+    w = wl.Workload(f"bwd_{B}x{H}x{N}", "bwd", B, H, N, d, dtype, causal, seed=7 + N + d)
     inp = wl.make_inputs(w)
     grads = _gpu_grads(attn_lib, inp, w)
     refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), causal,
@@ -103,7 +104,7 @@ def test_bwd_argument_errors(attn_lib):
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     need = attn_lib.bwd_workspace_bytes(1, 1, 64, 128)
     args = lambda d, wsz: (p, p, p, p, p, pl, p, p, p, pw, wsz, 1, 1, 64, d, 1, 0.1, 1, s)  # noqa
-    assert L.attn_bwd(*args(64, need)) == 2            # d = 64 unsupported
+    assert L.attn_bwd(*args(80, need)) == 2            # d = 80 unsupported
     assert L.attn_bwd(*args(128, need - 1)) == 1       # workspace too small
     assert L.attn_bwd(*args(128, need)) == 0
     assert attn_lib.poll_status()[0] == 0

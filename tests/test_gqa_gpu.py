@@ -39,9 +39,10 @@ def test_gqa_forward_small(attn_lib, causal, dtype, d, B, Hq, Hkv, N):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
 @pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 4, 2, 300), (2, 4, 1, 257), (1, 6, 3, 640)])
-def test_gqa_backward_small(attn_lib, causal, B, Hq, Hkv, N):
-    w, q, k, v, do = _make(B, Hq, Hkv, N, 128, "bf16", seed=7 * N + Hkv)
+def test_gqa_backward_small(attn_lib, causal, dtype, d, B, Hq, Hkv, N):
+    w, q, k, v, do = _make(B, Hq, Hkv, N, d, dtype, seed=7 * N + Hkv + d)
     qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
     o, lse = attn_lib.fwd(qc, kc, vc, causal=causal, scale=w.scale)
     dq, dk, dv = attn_lib.bwd(qc, kc, vc, o, doc, lse, causal=causal, scale=w.scale)

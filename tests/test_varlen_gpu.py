@@ -44,10 +44,11 @@ def test_varlen_forward(attn_lib, causal, dtype, d, lengths, Hq, Hkv):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
 @pytest.mark.parametrize("lengths,Hq,Hkv", [(MIX, 4, 2), ([129, 0, 384, 1], 2, 2)])
-def test_varlen_backward(attn_lib, causal, lengths, Hq, Hkv):
-    inp = wl.make_varlen_inputs(lengths, Hq, Hkv, 128, "bf16", seed=3 * len(lengths) + Hkv)
-    scale = 128 ** -0.5
+def test_varlen_backward(attn_lib, causal, dtype, d, lengths, Hq, Hkv):
+    inp = wl.make_varlen_inputs(lengths, Hq, Hkv, d, dtype, seed=3 * len(lengths) + Hkv + d)
+    scale = d ** -0.5
     q, k, v, do, cu = (inp[n].cuda() for n in ("q", "k", "v", "do", "cu_seqlens"))
     o, lse = attn_lib.fwd_varlen(q, k, v, cu, max(lengths), causal=causal, scale=scale)
     dq, dk, dv = attn_lib.bwd_varlen(q, k, v, o, do, lse, cu, max(lengths), causal=causal,

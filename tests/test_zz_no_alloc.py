@@ -37,7 +37,8 @@ def _noalloc_fn(attn):
 
 def _call(fn, q, k, v, o, do, lse, dq, dk, dv, w, stream):
     return fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-              _ptr(dv), w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), 1, stream)
+              _ptr(dv), w.B, w.H, w.N, w.d, int(w.causal), float(w.scale),
+              1 if w.dtype == "bf16" else 0, stream)  # ATTN_BF16 / ATTN_F16
 
 
 def test_noalloc_backward_matches_attn_bwd_twice(attn_lib):
@@ -45,7 +46,8 @@ def test_noalloc_backward_matches_attn_bwd_twice(attn_lib):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     # two different problems in a row through the shared scratch array
     for w in (wl.Workload("na1", "bwd", 1, 4, 1000, 128, "bf16", True, seed=31),
-              wl.Workload("na2", "bwd", 2, 3, 4096, 128, "bf16", False, seed=32)):
+              wl.Workload("na2", "bwd", 2, 3, 4096, 128, "bf16", False, seed=32),
+              wl.Workload("na3", "bwd", 1, 2, 700, 64, "fp16", True, seed=33)):
         inp = wl.make_inputs(w)
         q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
         o, lse = attn_lib.fwd(q, k, v, causal=w.causal, scale=w.scale)
@@ -67,6 +69,6 @@ def test_noalloc_rejects_oversized_problems(attn_lib):
     lse = torch.zeros((1, 1, 16), dtype=torch.float32, device="cuda")
     big = wl.Workload("big", "bwd", 1, 1, MAX_ROWS + 1, 128, "bf16", True)
     assert _call(fn, x, x, x, x, x, lse, x, x, x, big, stream) == 1  # ATTN_ERR_INVALID_ARG
-    d64 = wl.Workload("d64", "bwd", 1, 1, 16, 64, "bf16", True)
-    assert _call(fn, x, x, x, x, x, lse, x, x, x, d64, stream) == 2  # ATTN_ERR_UNSUPPORTED
+    d80 = wl.Workload("d80", "bwd", 1, 1, 16, 80, "bf16", True)
+    assert _call(fn, x, x, x, x, x, lse, x, x, x, d80, stream) == 2  # ATTN_ERR_UNSUPPORTED
     assert attn_lib.poll_status()[0] == 0
