@@ -329,6 +329,45 @@ def gqa_timing(attn, st, w, stream, hkv, iters=10):
             "note": "grouped query heads, timed apart from the step (not in value)"}
 
 
+def head_dim_timing(attn, w, dev, stream, iters=10):
+    """Forward + backward at the other head dims (64 and 96) on the step's
+    B, H, N, dtype and masking, timed apart from the step.  Inputs are
+    standard normals drawn on the device from a seeded generator (timing
+    only; parity at these head dims is in the tests)."""
+    out = {}
+    g = torch.Generator(device=dev).manual_seed(1234)
+    for d in (64, 96):
+        wd = w.with_(d=d)
+        shape = (wd.B, wd.H, wd.N, d)
+        q, k, v, do = (torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+                       .to(torch.bfloat16) for _ in range(4))
+        o, lse = attn.fwd(q, k, v, causal=wd.causal, scale=wd.scale)
+        grads = attn.bwd(q, k, v, o, do, lse, causal=wd.causal, scale=wd.scale)
+        torch.cuda.synchronize()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        tf, tb = [], []
+        for _ in range(iters):
+            e[0].record(stream)
+            attn.fwd(q, k, v, causal=wd.causal, scale=wd.scale, out=o, lse=lse)
+            e[1].record(stream)
+            attn.bwd(q, k, v, o, do, lse, causal=wd.causal, scale=wd.scale, dq=grads[0],
+                     dk=grads[1], dv=grads[2])
+            e[2].record(stream)
+            torch.cuda.synchronize()
+            tf.append(e[0].elapsed_time(e[1]))
+            tb.append(e[1].elapsed_time(e[2]))
+        status = attn.poll_status()
+        if status[0] != 0:
+            raise RuntimeError(f"device status after the d={d} timing: {status}")
+        mf, mb = statistics.mean(tf), statistics.mean(tb)
+        out[f"d{d}"] = {"fwd_ms": round(mf, 4), "bwd_ms": round(mb, 4),
+                        "fwd_tflops": round(wd.fwd_flops() / (mf * 1e-3) / 1e12, 1),
+                        "bwd_tflops": round(wd.bwd_flops() / (mb * 1e-3) / 1e12, 1)}
+        del q, k, v, do, o, lse, grads
+    out["note"] = "bf16, the step's B, H, N and masking; timed apart from the step (not in value)"
+    return out
+
+
 def varlen_timing(attn, dev, stream, iters=10):
     """Forward + backward on the packed variable-length batch (16 heads,
     d = 128, bf16, causal, 16384 tokens per head in the seeded length mix),
@@ -481,13 +520,14 @@ def run_gpu(args, rank, world, local_rank):
     split = split_kv_timing(attn, st, w, stream, n_split=SPLIT_KV_N)
     gqa = gqa_timing(attn, st, w, stream, GQA_KV_HEADS) if "bwd" in comps else None
     varlen = varlen_timing(attn, dev, stream) if "bwd" in comps else None
+    head_dims = head_dim_timing(attn, w, dev, stream) if "bwd" in comps else None
 
     step_flops = sum(flops[c] for c in comps)
     ms_step = ms_total / args.steps
     if world > 1:
         ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
     return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks, split=split,
-                gqa=gqa, varlen=varlen,
+                gqa=gqa, varlen=varlen, head_dims=head_dims,
                 flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
                 launches=sum(LAUNCHES[c] for c in comps) * args.steps)
 
@@ -626,6 +666,8 @@ def main():
         line["gqa"] = r["gqa"]
     if r.get("varlen"):
         line["varlen"] = r["varlen"]
+    if r.get("head_dims"):
+        line["head_dims"] = r["head_dims"]
     if not args.no_cpu_baseline:
         tf, dt, heads, cores = cpu_oracle_sample()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores,

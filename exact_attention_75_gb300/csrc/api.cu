@@ -139,7 +139,7 @@ cudaError_t launch_varlen_check(const int* cu, int n_seq, int total, int max_seq
 
 bool shape_ok(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return false;
-  if (d != 64 && d != 128) return false;
+  if (d != 64 && d != 96 && d != 128) return false;
   const int64_t bh = (int64_t)B * H;
   if (bh > (1 << 30) || N > (1 << 28)) return false;
   return bh * N * d < (int64_t)1 << 40;
@@ -197,7 +197,7 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
@@ -291,7 +291,7 @@ attn_status attn_merge(const void* o_part, const float* lse_part, int n_split, v
   if (n_split < 1 || n_split > 256) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
@@ -339,7 +339,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(varlen ? 1 : B, H, N, d))
     return ATTN_ERR_INVALID_ARG;

@@ -55,9 +55,10 @@ constexpr int kWarpRelay = 10;
 constexpr uint32_t kBarRelay = 3;  // named barrier: relay warp + issuer warp (64 threads)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStatusLayout = 5;  // shared memory not 1024-byte aligned
-// Bytes of a 128-row tile of 16-bit values with D columns.
+// Bytes of a 128-row tile of 16-bit values with D columns (padded to a
+// multiple of 64).
 template <int D>
-constexpr int kTileBytes = 128 * D * 2;
+constexpr int kTileBytes = 128 * kPaddedD<D> * 2;
 
 // Column of the K-step kk (16 values of the contraction index) of a 16-bit
 // operand that the two warpgroups wrote into the first 32 columns of their
@@ -70,12 +71,14 @@ __device__ __forceinline__ uint32_t pack16x2(bool bf16, float lo, float hi) {
   return bf16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
 
-// Loads a 128 x D 16-bit tile (D/64 boxes of 64 columns) with TMA.
+// Loads a 128 x D 16-bit tile (boxes of 64 columns; columns past D are
+// zero-filled) with TMA.
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                           int row0, int bh) {
 #pragma unroll
-  for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * 16384, map, bar, 64 * h, row0, bh);
+  for (int h = 0; h < kPaddedD<D> / 64; ++h)
+    tma_load_3d(dst + h * 16384, map, bar, 64 * h, row0, bh);
 }
 
 // ============================================================ dK, dV kernel ===
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
-      constexpr uint32_t kIdKV = idesc_f16(128, D, BF16, false, true);  // dV, dK
+      constexpr uint32_t kIdKV = idesc_f16(128, kPaddedD<D>, BF16, false, true);  // dV, dK
       uint32_t st_it = 0;
       bool aborted = false;
       // K and V as K-major A operands of S^T / dP^T.
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nothing), so every rendezvous pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);  // S, dP
-      constexpr uint32_t kIdQ = idesc_f16(128, D, BF16, false, true);     // dQ
+      constexpr uint32_t kIdQ = idesc_f16(128, kPaddedD<D>, BF16, false, true);  // dQ
       uint32_t k_it = 0, v_it = 0, step_it = 0;
       bool aborted = false;
       const uint64_t qd = kmajor_base(sbase + L::kQ), dod = kmajor_base(sbase + L::kDO);
@@ -917,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;                 // key half of every step
     const int r = threadIdx.x & 127;         // TMEM lane: query row
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t dq_addr = tbase + lane_base + kColDQ + (D / 2) * h;
+    const uint32_t dq_addr = tbase + lane_base + kColDQ;
     const float sl2 = p.scale_log2;
     uint32_t unit_it = 0, step_it = 0;
     bool ok = true;
@@ -1017,9 +1020,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++unit_it;
       tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D + (D / 2) * h);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D);
+      // 32-column chunks alternate between the two warpgroups.
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
+      for (int cc = 0; cc < (D / 32 + 1) / 2; ++cc) {
+        const int c = 2 * cc + h;
+        if (c >= D / 32) break;  // warp-uniform
         uint32_t raw[32];
         tmem_ld32_sync(dq_addr + 32 * c, raw);
         uint32_t pk[16];
@@ -1048,19 +1054,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================================================ D kernel ===
 
-// D_i = sum_c dO_ic O_ic with one warp per row (D/32 values per lane, then a
+// D_i = sum_c dO_ic O_ic with one warp per row (up to 4 values per lane, then a
 // butterfly of warp shuffles).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                      const uint16_t* __restrict__ dout,
                                                      float* __restrict__ delta, long rows) {
-  constexpr int W = D / 64;  // 32-bit words (two values each) per lane
+  constexpr int W = (D + 63) / 64;  // 32-bit words (two values each) per lane, at most
   const long warp0 = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   for (long row = warp0; row < rows; row += nwarps) {
     uint32_t aw[W], bw[W];
-    if constexpr (W == 2) {
+    if constexpr (D == 128) {  // the whole row in one 8-byte load per lane
       const uint2 a = reinterpret_cast<const uint2*>(o + row * D)[lane];
       const uint2 b = reinterpret_cast<const uint2*>(dout + row * D)[lane];
       aw[0] = a.x;
@@ -1068,8 +1074,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
       bw[0] = b.x;
       bw[1] = b.y;
     } else {
-      aw[0] = reinterpret_cast<const uint32_t*>(o + row * D)[lane];
-      bw[0] = reinterpret_cast<const uint32_t*>(dout + row * D)[lane];
+      // word lane + 32 e of the row (D / 2 words; D = 96 leaves lanes 16-31
+      // without a second word)
+#pragma unroll
+      for (int e = 0; e < W; ++e) {
+        const int wi = lane + 32 * e;
+        const bool in = wi < D / 2;
+        aw[e] = in ? reinterpret_cast<const uint32_t*>(o + row * D)[wi] : 0u;
+        bw[e] = in ? reinterpret_cast<const uint32_t*>(dout + row * D)[wi] : 0u;
+      }
     }
     float acc = 0.f;
 #pragma unroll
@@ -1139,6 +1152,7 @@ cudaError_t launch_all(const BwdLaunch& a) {
 
 cudaError_t launch_bwd(const BwdLaunch& a) {
   if (a.d == 64) return a.bf16 ? launch_all<64, true>(a) : launch_all<64, false>(a);
+  if (a.d == 96) return a.bf16 ? launch_all<96, true>(a) : launch_all<96, false>(a);
   return a.bf16 ? launch_all<128, true>(a) : launch_all<128, false>(a);
 }
 

@@ -44,7 +44,7 @@ struct BwdLaunch {
   int num_sms;
   cudaStream_t stream;
   bool causal, bf16;
-  int d = 128;            // head dimension: 64 or 128
+  int d = 128;            // head dimension: 64, 96 or 128
 };
 
 cudaError_t launch_bwd(const BwdLaunch& a);

@@ -57,7 +57,7 @@ constexpr int kPrecF16 = 0, kPrecBF16 = 1, kPrecE4M3 = 2;
 
 template <int D, bool FP8>
 struct FwdLayout {
-  static constexpr int kTileBytes = 128 * D * (FP8 ? 1 : 2);  // 128 rows x D values
+  static constexpr int kTileBytes = 128 * kPaddedD<D> * (FP8 ? 1 : 2);  // 128 rows, padded
   static constexpr int kSlots = (FP8 || D == 64) ? 8 : 4;     // K/V ring depth (tiles)
   static constexpr int kQOff = 0;
   static constexpr int kKvOff = 2 * kTileBytes;
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, w.row0 + (2 * w.qp + t) * 128, w.zq);
           } else {
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h)
+            for (int h = 0; h < kPaddedD<D> / 64; ++h)
               tma_load_3d(dst + h * 16384, &tmQ, bar(L::kQFull + t), h * 64,
                           w.row0 + (2 * w.qp + t) * 128, w.zq);
           }
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(dst, &tmV, bar(L::kKvFull + slot), (w.kb0 + j) * 128, 0, w.zkv);
             } else {
 #pragma unroll
-              for (int h = 0; h < D / 64; ++h)
+              for (int h = 0; h < kPaddedD<D> / 64; ++h)
                 tma_load_3d(dst + h * 16384, which ? &tmV : &tmK, bar(L::kKvFull + slot),
                             h * 64, w.row0 + (w.kb0 + j) * 128, w.zkv);
             }
@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdS =
         FP8 ? idesc_e4m3(128, 128, false, false) : idesc_f16(128, 128, BF16, false, false);
     constexpr uint32_t kIdO =
-        FP8 ? idesc_e4m3(128, D, false, false) : idesc_f16(128, D, BF16, false, true);
+        FP8 ? idesc_e4m3(128, D, false, false)
+            : idesc_f16(128, kPaddedD<D>, BF16, false, true);
     uint32_t kv_it = 0;
     bool aborted = false;
     bool issued = false;
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // O_t += P_t V_j  (A = P from tensor memory)
     auto issue_pv = [&](int t, uint32_t vaddr, uint32_t acc0) {
-      const uint32_t ocol = tbase + 256 + D * t;
+      const uint32_t ocol = tbase + 256 + kPaddedD<D> * t;
       const uint32_t pcol = tbase + 128 * t;
       if constexpr (FP8) {
         const uint64_t vd = kmajor_base(vaddr);
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x & 127;         // row within the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_addr = tbase + lane_base + 128u * t;
-    const uint32_t o_addr = tbase + lane_base + 256u + D * t;
+    const uint32_t o_addr = tbase + lane_base + 256u + kPaddedD<D> * t;
     const float sl2 = p.scale_log2;
     uint32_t s_it = 0, o_it = 0;
     // After an abort the schedule is still walked to the end with every wait
@@ -676,6 +677,9 @@ cudaError_t launch_fwd(const FwdLaunch& a, int d, bool causal, bool bf16) {
   if (d == 128)
     return bf16 ? launch_dc<128, kPrecBF16>(q, k, v, a.params, a.num_ctas, a.stream, causal)
                 : launch_dc<128, kPrecF16>(q, k, v, a.params, a.num_ctas, a.stream, causal);
+  if (d == 96)
+    return bf16 ? launch_dc<96, kPrecBF16>(q, k, v, a.params, a.num_ctas, a.stream, causal)
+                : launch_dc<96, kPrecF16>(q, k, v, a.params, a.num_ctas, a.stream, causal);
   return bf16 ? launch_dc<64, kPrecBF16>(q, k, v, a.params, a.num_ctas, a.stream, causal)
               : launch_dc<64, kPrecF16>(q, k, v, a.params, a.num_ctas, a.stream, causal);
 }

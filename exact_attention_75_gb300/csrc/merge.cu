@@ -10,7 +10,8 @@
 // at all gets O = 0 and LSE = -inf.
 //
 // d/8 lanes per row (8 values, one 16-byte read of each split's row per
-// lane), so a warp merges 32/(d/8) rows at once; the splits' rows are read
+// lane), so a warp merges 32/(d/8) rows at once (rounded down: at d = 96
+// lanes 24-31 idle); the splits' rows are read
 // four at a time so their loads are in flight together; grid-stride over
 // rows; arithmetic in fp32.
 #include <cuda_runtime.h>
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__
   const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
   for (long row0 = warp0 * kRowsPerWarp; row0 < rows; row0 += nwarps * kRowsPerWarp) {
     const long row = row0 + sub;
-    const bool live = row < rows;
+    const bool live = sub < kRowsPerWarp && row < rows;
     const long rrow = live ? row : rows - 1;  // in-range address for idle lanes
     float m = -INFINITY;
     for (int s = 0; s < n_split; ++s) m = fmaxf(m, lse_part[(size_t)s * rows + rrow]);
@@ -118,6 +119,7 @@ cudaError_t launch_d(const MergeLaunch& a) {
 }  // namespace
 
 cudaError_t launch_merge(const MergeLaunch& a) {
+  if (a.d == 96) return launch_d<96>(a);
   return a.d == 128 ? launch_d<128>(a) : launch_d<64>(a);
 }
 

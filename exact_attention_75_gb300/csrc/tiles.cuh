@@ -1,7 +1,11 @@
 // Shared-memory tile conventions shared by the attention kernels.
 //
 // A 16-bit [128 rows][d] tile is loaded by TMA with the 128-byte swizzle as
-// d/64 column halves, each [128 rows][64 values] = 16 KB, 1024-byte aligned.
+// column halves, each [128 rows][64 values] = 16 KB, 1024-byte aligned.  A
+// head dim that is not a multiple of 64 (d = 96) occupies the columns of the
+// next multiple: TMA fills the columns past d with zeros, so products that
+// contract over d stop at d, and products with d outputs per row run over the
+// padded width and produce zeros there.
 #pragma once
 
 #include <cstdint>
@@ -9,6 +13,10 @@
 #include "sm103_ptx.cuh"
 
 namespace attn {
+
+// Columns a 128-row tile of head dim D occupies in shared and tensor memory.
+template <int D>
+constexpr int kPaddedD = (D + 63) / 64 * 64;
 
 // Cheap K-step addressing for the MMA issuer.  A single thread issues every
 // tcgen05.mma of a CTA, so building descriptors from scratch per instruction

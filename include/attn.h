@@ -20,8 +20,9 @@
  *  - Layout: Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d] row-major and
  *    contiguous (d innermost); LSE and the delta vector D are [B, H, N].
  *    All pointers are DEVICE pointers, 16-byte aligned (TMA requirement).
- *  - Shapes: d in {64, 128}; N >= 1 (any N: partial tiles are zero-filled
- *    on load and masked); B, H >= 1; B*H*N*d must fit in 2^31 elements.
+ *  - Shapes: d in {64, 96, 128} (the FP8 entry points: as stated there);
+ *    N >= 1 (any N: partial tiles are zero-filled on load and masked);
+ *    B, H >= 1; B*H*N*d must fit in 2^31 elements.
  *  - Causal masking is top-left aligned: key j is visible to query i iff
  *    j <= i.  `scale` multiplies QK^T (1/sqrt(d) in the usual case).
  *  - LSE is the natural log of sum_j exp(scale * q_i . k_j) over the visible
@@ -111,7 +112,7 @@ attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_
  *   o_part   : [n_split, B, H, N, d] fp16/bf16 (dtype), read only.
  *   lse_part : [n_split, B, H, N] fp32, read only.
  *   o        : [B, H, N, d] dtype, written;  lse : [B, H, N] fp32, written.
- * d in {64, 128}; 1 <= n_split <= 256.
+ * d in {64, 96, 128}; 1 <= n_split <= 256.
  * Cite: the FlashAttention-2 review, "Insights" (the log-sum-exp is all that
  * has to be kept besides O); the combine formula follows from the softmax
  * definition over the union of the key sets.
@@ -136,7 +137,7 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *   workspace        : >= attn_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte
  *                      aligned, caller-owned; contents on entry are ignored
  *                      and on return are unspecified.
- * d in {64, 128} (ATTN_ERR_UNSUPPORTED otherwise).  dK, dV (per key tile)
+ * d in {64, 96, 128} (ATTN_ERR_UNSUPPORTED otherwise).  dK, dV (per key tile)
  * and dQ (per query tile) are each
  * accumulated in fp32 by one CTA in a fixed order, so the results are the
  * same from run to run.
@@ -178,7 +179,7 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
  * ATTN_ERR_INVALID_ARG in the status word (attn_poll_device_status returns
  * it; the block field of `detail` holds the first bad index).  Every
  * sequence is clamped into [0, total) and to max_seqlen rows, so a bad array
- * gives wrong results but no access outside the tensors.  d in {64, 128}.
+ * gives wrong results but no access outside the tensors.  d in {64, 96, 128}.
  * Cite: the FlashAttention-2 review, "Discussion Points" (the decoding /
  * KV-cache access pattern: many sequences of their own lengths); per
  * sequence the computation is attn_fwd's.
@@ -193,7 +194,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
  * dv [Hkv, total, d]; lse [Hq, total] from attn_fwd_varlen.  workspace: >=
  * attn_bwd_workspace_bytes(1, Hq, total, d) bytes, 256-byte aligned.  Rows of
  * dq, dk, dv outside every sequence (none when the offsets are valid) are
- * not written.  d in {64, 128}.  Offsets, checks and errors as in
+ * not written.  d in {64, 96, 128}.  Offsets, checks and errors as in
  * attn_fwd_varlen.
  * Cite: as attn_bwd and attn_fwd_varlen.
  */
@@ -214,7 +215,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
  * same dQ, dK, dV as attn_bwd, with the same arguments minus the workspace;
  * the scratch (the fp32 delta vector) lives in a fixed device array inside
  * the library.
- *   Limit: B*H*N <= 4194304 query rows and d in {64, 128}; larger problems return
+ *   Limit: B*H*N <= 4194304 query rows and d in {64, 96, 128}; larger problems return
  *   ATTN_ERR_INVALID_ARG, other head dims ATTN_ERR_UNSUPPORTED.
  *   Memory: the array (16 MB) is part of the library image and is held on
  *   every GPU that loads the library until the process exits.
@@ -238,7 +239,8 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
  *   scales  : [B,H,ceil(N/block_rows)] fp32: s = amax/448 over each block of
  *             `block_rows` rows x d columns (s = 1 if the block is all zero);
  *             codes are E4M3(x/s), round to nearest even, saturating.
- *   block_rows : 64 (the only supported value).
+ *   block_rows : 64 (the only supported value);  d in {64, 128} (the
+ *             rotation is a Walsh-Hadamard transform of power-of-two size).
  *   hadamard_signs : NULL (no rotation) or a DEVICE array of d int8 values,
  *             each +1 or -1.
  *   write_transposed : 0 or 1; 1 requires N % 16 == 0.

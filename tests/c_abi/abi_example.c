@@ -87,7 +87,7 @@ int main(void) {
   for (int i = 0; i < N; ++i)
     if (!isfinite(lse[i])) ++bad;
   /* an invalid argument is rejected before any launch */
-  if (attn_fwd(dev[0], dev[1], dev[2], dev[3], lse_d, 1, 1, N, 96, 1, scale, ATTN_F16, NULL) ==
+  if (attn_fwd(dev[0], dev[1], dev[2], dev[3], lse_d, 1, 1, N, 80, 1, scale, ATTN_F16, NULL) ==
       ATTN_OK)
     ++bad;
   for (int t = 0; t < 4; ++t) cudaFree(dev[t]);

@@ -44,7 +44,7 @@ def test_status_strings_and_workspace_size_without_gpu(lib):
     want = B * H * N * 4  # the fp32 delta vector D, 256-byte multiple here
     assert lib.attn_bwd_workspace_bytes(B, H, N, d) == want
     assert lib.attn_bwd_workspace_bytes(0, 1, 1, 128) == 0
-    assert lib.attn_bwd_workspace_bytes(1, 1, 1, 96) == 0
+    assert lib.attn_bwd_workspace_bytes(1, 1, 1, 80) == 0
     assert lib.attn_bwd_workspace_bytes(1, 1, 3, 128) == 256  # rounded up
 
 

@@ -47,7 +47,7 @@ def _check(w, grads, refs, heads=None):
         assert err <= REL_TOL, (w.name, name, err)
 
 
-@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("d", [128, 64, 96])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 17), (1, 1, 128), (2, 1, 129),

@@ -48,7 +48,7 @@ def test_tiny_fp16_causal_workload(attn_lib):
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 17), (2, 1, 128), (1, 3, 129), (2, 2, 255),
                                    (1, 2, 256), (1, 1, 300), (1, 2, 513), (2, 1, 1000)])
@@ -141,7 +141,7 @@ def test_invalid_arguments_rejected_before_launch(attn_lib):
     lse = torch.zeros((1, 1, 64), dtype=torch.float32, device="cuda")
     p, pl = ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(lse.data_ptr())
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    assert L.attn_fwd(p, p, p, p, pl, 1, 1, 64, 96, 0, 0.1, 0, s) == 2      # d unsupported
+    assert L.attn_fwd(p, p, p, p, pl, 1, 1, 64, 80, 0, 0.1, 0, s) == 2      # d unsupported
     assert L.attn_fwd(p, p, p, p, pl, 1, 1, 0, 64, 0, 0.1, 0, s) == 1       # N = 0
     assert L.attn_fwd(None, p, p, p, pl, 1, 1, 64, 64, 0, 0.1, 0, s) == 1   # null
     mis = ctypes.c_void_p(q.data_ptr() + 2)

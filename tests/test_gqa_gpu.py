@@ -27,7 +27,7 @@ def _make(B, Hq, Hkv, N, d, dtype, seed):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64), ("bf16", 96)])
 @pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 4, 2, 300), (2, 4, 1, 257), (1, 8, 2, 513)])
 def test_gqa_forward_small(attn_lib, causal, dtype, d, B, Hq, Hkv, N):
     w, q, k, v, _ = _make(B, Hq, Hkv, N, d, dtype, seed=N + Hkv)
@@ -39,7 +39,7 @@ def test_gqa_forward_small(attn_lib, causal, dtype, d, B, Hq, Hkv, N):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64), ("bf16", 96)])
 @pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 4, 2, 300), (2, 4, 1, 257), (1, 6, 3, 640)])
 def test_gqa_backward_small(attn_lib, causal, dtype, d, B, Hq, Hkv, N):
     w, q, k, v, do = _make(B, Hq, Hkv, N, d, dtype, seed=7 * N + Hkv + d)

@@ -37,7 +37,7 @@ def _check_partials(Op, Lp, O_ref, L_ref):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,N,n_split", [(1, 2, 300, 2), (2, 1, 513, 3), (1, 1, 1000, 8),
                                            (1, 2, 256, 5), (1, 1, 129, 1)])
@@ -56,7 +56,7 @@ def test_split_partials_and_merge_small(attn_lib, dtype, d, causal, B, H, N, n_s
     assert np.max(np.abs(to64(L) - L_ref)) <= LSE_TOL
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 def test_merge_kernel_vs_oracle_merge(attn_lib, d):
     """The merge alone on synthetic partials: random O_s, LSE_s of spread
     magnitudes, some -inf (a split without keys) and one all -inf row."""

@@ -29,7 +29,7 @@ def _run_fwd(attn, inp, max_seqlen, causal, scale):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64), ("bf16", 96)])
 @pytest.mark.parametrize("lengths,Hq,Hkv", [(MIX, 4, 2), (MIX, 2, 2), ([700], 2, 1),
                                             ([256, 256, 256], 3, 3)])
 def test_varlen_forward(attn_lib, causal, dtype, d, lengths, Hq, Hkv):
@@ -44,7 +44,7 @@ def test_varlen_forward(attn_lib, causal, dtype, d, lengths, Hq, Hkv):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64), ("bf16", 96)])
 @pytest.mark.parametrize("lengths,Hq,Hkv", [(MIX, 4, 2), ([129, 0, 384, 1], 2, 2)])
 def test_varlen_backward(attn_lib, causal, dtype, d, lengths, Hq, Hkv):
     inp = wl.make_varlen_inputs(lengths, Hq, Hkv, d, dtype, seed=3 * len(lengths) + Hkv + d)

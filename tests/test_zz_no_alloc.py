@@ -47,7 +47,8 @@ def test_noalloc_backward_matches_attn_bwd_twice(attn_lib):
     # two different problems in a row through the shared scratch array
     for w in (wl.Workload("na1", "bwd", 1, 4, 1000, 128, "bf16", True, seed=31),
               wl.Workload("na2", "bwd", 2, 3, 4096, 128, "bf16", False, seed=32),
-              wl.Workload("na3", "bwd", 1, 2, 700, 64, "fp16", True, seed=33)):
+              wl.Workload("na3", "bwd", 1, 2, 700, 64, "fp16", True, seed=33),
+              wl.Workload("na4", "bwd", 2, 1, 390, 96, "bf16", True, seed=34)):
         inp = wl.make_inputs(w)
         q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
         o, lse = attn_lib.fwd(q, k, v, causal=w.causal, scale=w.scale)
