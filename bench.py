@@ -368,6 +368,88 @@ def head_dim_timing(attn, w, dev, stream, iters=10):
     return out
 
 
+def _timed(fn, stream, flush, iters, warmup=3):
+    """Per-launch device times (ms) of fn on the stream, L2 flushed before
+    each launch (outside the timed region)."""
+    for _ in range(warmup):
+        fn()
+    ts = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(iters):
+        flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return ts
+
+
+def _summary(ts):
+    q1, q2, q3 = statistics.quantiles(ts, n=4)
+    return {"ms_median": round(q2, 4), "ms_iqr": [round(q1, 4), round(q3, 4)]}
+
+
+def sweep_timing(attn, dev, stream, iters=20):
+    """Forward at every configuration of the pages' workloads besides the
+    step: the 256-token fp16 case, the fp16 d=64 and bf16 d=128 (inputs x0.5)
+    sweeps over N with B*N = 16384, causal and not.  Inputs are seeded
+    standard normals drawn on the device (timing only; parity is in the
+    tests); L2 is flushed before every launch.  GB/s counts the algorithmic
+    bytes (read Q, K, V, write O once; LSE fp32)."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    points = [wl.TINY_FWD_FP16]
+    for causal in (True, False):
+        points += wl.sweep_d64(causal)
+    for causal in (True, False):
+        points += wl.sweep_d128(causal)
+    out = []
+    for w in points:
+        shape = (w.B, w.H, w.N, w.d)
+        q, k, v = ((torch.randn(shape, generator=g, device=dev) * w.input_scale)
+                   .to(w.torch_dtype) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        ts = _timed(lambda: attn.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse),
+                    stream, flush, iters)
+        status = attn.poll_status()
+        if status[0] != 0:
+            raise RuntimeError(f"device status after {w.name}: {status}")
+        r = _summary(ts)
+        nbytes = 4 * w.B * w.H * w.N * w.d * 2 + 4 * w.B * w.H * w.N
+        r.update({"workload": w.name, "dtype": w.dtype, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                  "causal": w.causal,
+                  "tflops": round(w.fwd_flops() / (r["ms_median"] * 1e-3) / 1e12, 1),
+                  "gbs": round(nbytes / (r["ms_median"] * 1e-3) / 1e9, 1)})
+        out.append(r)
+        del q, k, v, o, lse
+    return out
+
+
+def tensor_peaks(dev, stream, iters=20):
+    """Dense 8192^3 products through the libraries, the same way for both
+    types: bf16 torch.matmul and E4M3 torch._scaled_mm (unit scales, bf16
+    output).  A denominator for the E4M3 forward, not part of the path."""
+    M = 8192
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    a = torch.randn(M, M, device=dev).to(torch.bfloat16)
+    b = torch.randn(M, M, device=dev).to(torch.bfloat16)
+    ts = _timed(lambda: torch.matmul(a, b), stream, flush, iters)
+    res["bf16_tflops"] = round(2 * M ** 3 / (statistics.median(ts) * 1e-3) / 1e12, 1)
+    try:
+        a8, b8 = a.to(torch.float8_e4m3fn), b.to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        ts = _timed(lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one,
+                                             out_dtype=torch.bfloat16), stream, flush, iters)
+        res["e4m3_tflops"] = round(2 * M ** 3 / (statistics.median(ts) * 1e-3) / 1e12, 1)
+    except Exception as e:  # the library may not offer the product on this build
+        res["e4m3_unavailable"] = str(e).splitlines()[0][:200]
+    res["note"] = "8192^3, median of 20 launches, L2 flushed; burst"
+    return res
+
+
 def varlen_timing(attn, dev, stream, iters=10):
     """Forward + backward on the packed variable-length batch (16 heads,
     d = 128, bf16, causal, 16384 tokens per head in the seeded length mix),
@@ -566,6 +648,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweeps", action="store_true",
+                    help="time the forward at every configuration and sweep point of the "
+                         "workloads (one GPU) and print them instead of the step line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -575,6 +660,25 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     peaks = load_peaks()
     w = WORKLOAD
+
+    if args.sweeps and args.impl == "gb300":
+        if rank != 0:
+            return
+        import exact_attention_75_gb300 as attn
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        stream = torch.cuda.current_stream()
+        sampler = ClockSampler(local_rank)
+        sampler.start()
+        sweeps = sweep_timing(attn, dev, stream)
+        clocks = sampler.stop()
+        line = {"metric": "attention fwd TFLOP/s per configuration", "impl": "gb300",
+                "unit": "TFLOP/s", "higher_is_better": True, "n_gpus": 1, "data": "synthetic",
+                "l2": "flushed (256 MiB write) before every launch", "clocks": clocks,
+                "peaks": {"measured": peaks, "this_run": tensor_peaks(dev, stream)},
+                "sweeps": sweeps}
+        print(json.dumps(line), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:
