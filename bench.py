@@ -450,6 +450,45 @@ def tensor_peaks(dev, stream, iters=20):
     return res
 
 
+def decode_timing(attn, dev, stream, peaks, iters=20):
+    """Decoding against a key/value cache, timed apart from the step: one
+    query per sequence, 16 sequences x 16 heads, an 8192-row bf16 d=128
+    cache, split over the keys into 4 runs (attn_fwd_kv) and merged
+    (attn_merge).  HBM-bound: the algorithmic bytes are the cache's K and V
+    read once (plus q, the partials and O, under 0.1 %).  Inputs are seeded
+    standard normals drawn on the device (timing only; parity is in the
+    tests); L2 is flushed before every call."""
+    w = wl.DECODE_BF16_D128
+    g = torch.Generator(device=dev).manual_seed(0)
+    q = torch.randn((w.B, w.H, wl.DECODE_NQ, w.d), generator=g, device=dev).to(torch.bfloat16)
+    k, v = (torch.randn((w.B, w.H, w.N, w.d), generator=g, device=dev).to(torch.bfloat16)
+            for _ in range(2))
+    Op, Lp = attn.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal)
+    O, L = attn.merge(Op, Lp)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        attn.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal, out=Op, lse=Lp)
+        attn.merge(Op, Lp, out=O, lse=L)
+
+    ts = _timed(step, stream, flush, iters)
+    status = attn.poll_status()
+    if status[0] != 0:
+        raise RuntimeError(f"device status after the decode timing: {status}")
+    r = _summary(ts)
+    kv_bytes = 2 * w.B * w.H * w.N * w.d * 2
+    gbs = kv_bytes / (r["ms_median"] * 1e-3) / 1e9
+    r.update({"workload": w.name, "n_split": wl.DECODE_SPLITS, "queries": wl.DECODE_NQ,
+              "gbs": round(gbs, 1),
+              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                           "algorithmic_bytes": kv_bytes},
+              "note": "fwd_kv (4 key splits) + merge, L2 flushed, timed apart from the step "
+                      "(not in value)"})
+    del q, k, v, Op, Lp, O, L
+    return r
+
+
 def varlen_timing(attn, dev, stream, iters=10):
     """Forward + backward on the packed variable-length batch (16 heads,
     d = 128, bf16, causal, 16384 tokens per head in the seeded length mix),
@@ -603,13 +642,14 @@ def run_gpu(args, rank, world, local_rank):
     gqa = gqa_timing(attn, st, w, stream, GQA_KV_HEADS) if "bwd" in comps else None
     varlen = varlen_timing(attn, dev, stream) if "bwd" in comps else None
     head_dims = head_dim_timing(attn, w, dev, stream) if "bwd" in comps else None
+    decode = decode_timing(attn, dev, stream, load_peaks())
 
     step_flops = sum(flops[c] for c in comps)
     ms_step = ms_total / args.steps
     if world > 1:
         ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
     return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks, split=split,
-                gqa=gqa, varlen=varlen, head_dims=head_dims,
+                gqa=gqa, varlen=varlen, head_dims=head_dims, decode=decode,
                 flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
                 launches=sum(LAUNCHES[c] for c in comps) * args.steps)
 
@@ -772,6 +812,8 @@ def main():
         line["varlen"] = r["varlen"]
     if r.get("head_dims"):
         line["head_dims"] = r["head_dims"]
+    if r.get("decode"):
+        line["decode"] = r["decode"]
     if not args.no_cpu_baseline:
         tf, dt, heads, cores = cpu_oracle_sample()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores,

@@ -19,7 +19,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["AttnError", "lib", "lib_path", "fwd", "fwd_split", "merge", "bwd", "fwd_varlen",
+__all__ = ["AttnError", "lib", "lib_path", "fwd", "fwd_split", "fwd_kv", "merge", "bwd", "fwd_varlen",
            "bwd_varlen", "bwd_workspace_bytes", "quantize_fp8", "fwd_fp8", "poll_status", "set_wait_limit_us",
            "selftest_wait_timeout", "num_sms", "STATUS"]
 
@@ -57,6 +57,7 @@ def lib() -> ctypes.CDLL:
         "attn_fwd": ([vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp], i),
         "attn_fwd_split": ([vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp], i),
         "attn_fwd_gqa": ([vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp], i),
+        "attn_fwd_kv": ([vp] * 5 + [i] * 8 + [f, i, vp], i),
         "attn_bwd_gqa": ([vp] * 10 + [sz, i, i, i, i, i, i, f, i, vp], i),
         "attn_merge": ([vp, vp, i, vp, vp, i, i, i, i, i, vp], i),
         "attn_fwd_varlen": ([vp] * 6 + [i, i, i, i, i, i, i, f, i, vp], i),
@@ -174,6 +175,43 @@ def fwd_split(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_split: int,
                                   B, H, N, d, int(bool(causal)), float(scale), _dtype_code(q),
                                   _stream(q))
     _check(st, "attn_fwd_split")
+    return out, lse
+
+
+def fwd_kv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_split: int = 1,
+           causal: bool = False, scale: Optional[float] = None,
+           out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Nq queries (the last Nq positions) against an Nk-row key/value cache,
+    split over the keys: q [B,Hq,Nq,d], k, v [B,Hkv,Nk,d] (Hkv divides Hq,
+    Nq <= Nk).  Returns O_parts [n_split,B,Hq,Nq,d], LSE_parts
+    [n_split,B,Hq,Nq] (combine with merge; n_split = 1 holds the result).
+    causal: query i sees keys j <= i + Nk - Nq."""
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, Hq, Nq, d] and k, v [B, Hkv, Nk, d]")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = int(k.shape[1]), int(k.shape[2])
+    if k.shape[0] != B or k.shape[3] != d or Hq % Hkv != 0 or Nq > Nk:
+        raise ValueError("k, v must be [B, Hkv, Nk, d] with Hkv dividing Hq and Nk >= Nq")
+    for t in (q, k, v):
+        if not t.is_cuda or t.device != q.device or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous tensors of one dtype on one device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((n_split, B, Hq, Nq, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((n_split, B, Hq, Nq), dtype=torch.float32, device=q.device)
+    if tuple(out.shape) != (n_split, B, Hq, Nq, d) or out.dtype != q.dtype \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [n_split, B, Hq, Nq, d] tensor of q's dtype")
+    if tuple(lse.shape) != (n_split, B, Hq, Nq) or lse.dtype != torch.float32:
+        raise ValueError("lse must be a float32 [n_split, B, Hq, Nq] tensor")
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(n_split),
+                               B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+                               _dtype_code(q), _stream(q))
+    _check(st, "attn_fwd_kv")
     return out, lse
 
 

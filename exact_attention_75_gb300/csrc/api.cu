@@ -155,6 +155,7 @@ attn_status fill_fwd_common(FwdLaunch* a, DeviceInfo* di, int B, int H, int N, f
   p.status = di->status;
   p.BH = B * H;
   p.N = N;
+  p.Nk = N;
   p.n_qtiles = (N + 127) / 128;
   p.n_pairs = (p.n_qtiles + 1) / 2;
   p.n_kblocks = (N + 127) / 128;
@@ -182,10 +183,13 @@ namespace {
 // With cu_seqlens (device, B + 1 entries) the batch is B packed sequences of
 // at most max_seqlen rows: q, o are [H, N, d], k, v [Hkv, N, d], lse [H, N],
 // N the total rows.
+//
+// Nk > 0 (dense batches only) gives K and V their own row count Nk >= N:
+// the N queries are the last N positions of a sequence of Nk keys.
 attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                      int n_split, int B, int H, int Hkv, int N, int d, int causal, float scale,
                      attn_dtype dtype, void* stream, const int* cu_seqlens = nullptr,
-                     int max_seqlen = 0) {
+                     int max_seqlen = 0, int Nk = 0) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
   const bool varlen = cu_seqlens != nullptr;
@@ -199,6 +203,8 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+  if (Nk == 0) Nk = N;
+  if (Nk < N || (varlen && Nk != N) || !shape_ok(B, Hkv, Nk, d)) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
   if (st != ATTN_OK) return st;
@@ -209,11 +215,13 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   // tensor-map head index: (batch, head) for dense tensors, head for packed ones
   const int64_t zq = varlen ? H : BH, zkv = varlen ? Hkv : BHkv;
   if (!encode_3d(&a.tmQ, q, dt, 2, d, N, zq, 64, 128) ||
-      !encode_3d(&a.tmK, k, dt, 2, d, N, zkv, 64, 128) ||
-      !encode_3d(&a.tmV, v, dt, 2, d, N, zkv, 64, 128))
+      !encode_3d(&a.tmK, k, dt, 2, d, Nk, zkv, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, Nk, zkv, 64, 128))
     return ATTN_ERR_CUDA;
   fill_fwd_common(&a, di, B, H, N, scale, stream, o, lse);
   FwdParams& p = a.params;
+  p.Nk = Nk;
+  p.n_kblocks = (Nk + 127) / 128;
   p.heads_kv = Hkv;
   p.group = H / Hkv;
   if (varlen) {
@@ -275,6 +283,13 @@ attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, f
                          int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                          attn_dtype dtype, void* stream) {
   return fwd_impl(q, k, v, o, lse, 1, B, Hq, Hkv, N, d, causal, scale, dtype, stream);
+}
+
+attn_status attn_fwd_kv(const void* q, const void* k, const void* v, void* o_part,
+                        float* lse_part, int n_split, int B, int Hq, int Hkv, int Nq, int Nk,
+                        int d, int causal, float scale, attn_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o_part, lse_part, n_split, B, Hq, Hkv, Nq, d, causal, scale, dtype,
+                  stream, nullptr, 0, Nk);
 }
 
 attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_part,

@@ -77,7 +77,9 @@ struct Unit {
   int bhkv;   // key/value head (batch * heads_kv + head / group)
   int zq, zkv;  // tensor-map head index of Q / O and of K / V
   int row0;   // first row of the sequence in its head
-  int len;    // rows of the sequence
+  int len;    // query rows of the sequence
+  int klen;   // key rows of the sequence
+  int koff;   // causal: query row i sees keys j <= i + koff
   int nkb;    // its 128-row tiles (query tiles = key blocks)
   int split;  // key split of this unit (0 without a split)
   int kb0;    // first key block of the split
@@ -106,26 +108,31 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     const int s1 = min(max(__ldg(p.cu_seqlens + b + 1), s0), p.N);
     w.row0 = s0;
     w.len = min(s1 - s0, p.max_seqlen);
+    w.klen = w.len;
+    w.koff = 0;
     w.zq = hq;
     w.zkv = hq / p.group;
     w.bhkv = w.zkv;
   } else {
     w.row0 = 0;
     w.len = p.N;
+    w.klen = p.Nk;
+    w.koff = p.Nk - p.N;
     w.zq = w.bh;
     w.bhkv = b * p.heads_kv + hq / p.group;
     w.zkv = w.bhkv;
   }
-  w.nkb = (w.len + 127) >> 7;
+  w.nkb = (w.klen + 127) >> 7;
   w.kb0 = (w.split * w.nkb) / p.n_split;
   const int kb1 = ((w.split + 1) * w.nkb) / p.n_split;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int tile = 2 * w.qp + t;
-    if (tile >= w.nkb) {
+    if (tile * 128 >= w.len) {
       w.nb[t] = 0;
     } else {
-      const int visible = CAUSAL ? min(tile + 1, w.nkb) : w.nkb;
+      // causal: the tile's last row sees keys up to tile * 128 + 127 + koff
+      const int visible = CAUSAL ? min((tile * 128 + 127 + w.koff) / 128 + 1, w.nkb) : w.nkb;
       w.nb[t] = max(0, min(visible, kb1) - w.kb0);
     }
   }
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* const lbase = p.lse + w.split * p.lse_split;
       if (nb == 0) {
         // A query tile that sees no key of this split: O = 0, LSE = -inf.
-        if (tile < w.nkb && row < w.len) {
+        if (row < w.len) {
           const size_t grow = (size_t)w.zq * p.N + w.row0 + row;
           uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
@@ -499,11 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
         const int jk = w.kb0 + j;  // key block index
-        const bool diag = CAUSAL && (jk == tile);
-        const bool tail = (jk == w.nkb - 1) && (w.len & 127);
+        // blocks that reach past the tile's first row's last visible key
+        const bool diag = CAUSAL && (jk * 128 + 127 > tile * 128 + w.koff);
+        const bool tail = (jk == w.nkb - 1) && (w.klen & 127);
         if (diag || tail) {
           const int kbase = jk * 128;
-          const int lim = CAUSAL ? min(row, w.len - 1) : (w.len - 1);
+          const int lim = CAUSAL ? min(row + w.koff, w.klen - 1) : (w.klen - 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
@@ -611,7 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         aborted = !__all_sync(0xffffffffu, mbar_wait(bar(L::kOFull + t), opar, wd, 12));
       if (aborted) continue;
       tc_fence_after();
-      const float inv_l = (FP8 ? sv_max : 1.0f) / l;
+      // A row that sees no key of this split (a short query block against a
+      // longer cache) has l = 0: O = 0, LSE = -inf.
+      const float inv_l = l > 0.f ? (FP8 ? sv_max : 1.0f) / l : 0.f;
       const size_t grow = (size_t)w.zq * p.N + w.row0 + row;
       uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll

@@ -11,7 +11,11 @@ struct FwdParams {
   void* o;              // [B*H, N, D] 16-bit output
   float* lse;           // [B*H, N] fp32 output
   uint32_t* status;     // device status word
-  int BH, N;
+  int BH, N;            // N: query rows per head
+  // Key / value rows per head (= N except when a short block of queries
+  // attends to a longer key cache).  Causal masking is aligned at the
+  // bottom right: query row i sits at key position i + Nk - N.
+  int Nk;
   int n_qtiles;         // ceil(N / 128)
   int n_pairs;          // ceil(n_qtiles / 2): work units per head
   int n_kblocks;        // ceil(N / 128)

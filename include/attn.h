@@ -105,6 +105,28 @@ attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_
                            float scale, attn_dtype dtype, void* stream);
 
 /*
+ * Forward pass of a block of Nq queries against a longer key/value cache
+ * (decoding: Nq = 1, or a few draft tokens), split over the keys like
+ * attn_fwd_split and with grouped query heads like attn_fwd_gqa:
+ *   q        : [B,Hq,Nq,d], read only;  k, v : [B,Hkv,Nk,d], read only.
+ *   o_part   : [n_split,B,Hq,Nq,d] same dtype; lse_part [n_split,B,Hq,Nq]
+ *              fp32; written as in attn_fwd_split (n_split = 1: the final
+ *              O and LSE; otherwise combine them with attn_merge, whose
+ *              N is Nq).
+ *   1 <= Nq <= Nk.  The queries are the last Nq positions of the sequence:
+ *   with causal = 1 query i sees keys j <= i + Nk - Nq (so every query sees
+ *   at least Nk - Nq + 1 keys); causal = 0 sees all Nk keys.  Nq = Nk gives
+ *   attn_fwd_split (attn_fwd_gqa).  The split covers ceil(Nk/128) key
+ *   blocks.  Other arguments and errors as in attn_fwd_split and
+ *   attn_fwd_gqa.
+ * Cite: the FlashAttention-2 review, "Discussion Points" (decoding with a
+ * KV cache by a kernel that splits the keys, then combines the parts).
+ */
+attn_status attn_fwd_kv(const void* q, const void* k, const void* v, void* o_part,
+                        float* lse_part, int n_split, int B, int Hq, int Hkv, int Nq, int Nk,
+                        int d, int causal, float scale, attn_dtype dtype, void* stream);
+
+/*
  * Merge partial results over disjoint key sets (as written by
  * attn_fwd_split): per row, LSE = log sum_s exp(LSE_s) and
  * O = sum_s exp(LSE_s - LSE) O_s, computed in fp32 with the running maximum;

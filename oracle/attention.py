@@ -51,7 +51,7 @@ __all__ = [
     "rotation_matrix", "quantize_blocks", "dequantize_blocks", "rmse",
     "split_key_ranges", "attention_partial_head", "attention_split", "merge_partials",
     "kv_head_of", "attention_gqa", "attention_backward_gqa", "sequence_ranges",
-    "attention_varlen", "attention_backward_varlen",
+    "attention_varlen", "attention_backward_varlen", "attention_kv_head", "attention_kv",
 ]
 
 
@@ -260,6 +260,61 @@ def attention_backward_gqa(q, k, v, do, causal: bool, scale: float):
             dK[b, g] += dk
             dV[b, g] += dv
     return dQ, dK, dV
+
+
+# ---------------------------------------------------------------------------
+# A block of queries against a longer key/value cache (decoding)
+# ---------------------------------------------------------------------------
+# [FA2-review] "Discussion Points" raises decoding with a KV cache, served by
+# a kernel that splits the keys and combines the parts.  Reading: the Nq
+# queries are the last Nq positions of a sequence whose Nk >= Nq keys and
+# values are all cached, so with causal masking query i (position
+# Nk - Nq + i) sees keys j <= Nk - Nq + i; without it, all Nk keys.  The
+# split over the keys is the one of attention_split, over ceil(Nk/128) blocks.
+
+def attention_kv_head(q, k, v, causal: bool, scale: float, key_lo: int = 0,
+                      key_hi: Optional[int] = None):
+    """One head: q [Nq,d], k, v [Nk,d], keys restricted to [key_lo, key_hi).
+    Returns (O [Nq,d], LSE [Nq]); a row that sees no key of the range gets
+    LSE = -inf and O = 0."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    nq, nk = q.shape[0], k.shape[0]
+    key_hi = nk if key_hi is None else key_hi
+    O = np.zeros((nq, v.shape[1]), np.float64)
+    lse = np.full(nq, -np.inf)
+    if key_hi <= key_lo:
+        return O, lse
+    S = scores(q, k[key_lo:key_hi], scale)
+    allowed = np.ones(S.shape, dtype=bool)
+    if causal:
+        position = nk - nq + np.arange(nq)  # key position of each query
+        allowed = (key_lo + np.arange(key_hi - key_lo))[None, :] <= position[:, None]
+    has = allowed.any(axis=1)
+    if has.any():
+        P, l = masked_softmax(S[has], allowed[has])
+        O[has] = P @ v[key_lo:key_hi]
+        lse[has] = l
+    return O, lse
+
+
+def attention_kv(q, k, v, causal: bool, scale: float, n_split: int = 1, block: int = 128):
+    """q [B,Hq,Nq,d], k, v [B,Hkv,Nk,d] (grouped heads as attention_gqa) ->
+    O_parts [n_split,B,Hq,Nq,d], LSE_parts [n_split,B,Hq,Nq], split s over
+    the keys of split_key_ranges(Nk, n_split, block)."""
+    q = np.asarray(q, np.float64)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = np.shape(k)[1], np.shape(k)[2]
+    O = np.zeros((n_split, B, Hq, Nq, np.shape(v)[-1]), np.float64)
+    L = np.full((n_split, B, Hq, Nq), -np.inf)
+    for s, (lo, hi) in enumerate(split_key_ranges(Nk, n_split, block)):
+        for b in range(B):
+            for h in range(Hq):
+                g = kv_head_of(h, Hq, Hkv)
+                O[s, b, h], L[s, b, h] = attention_kv_head(q[b, h], k[b, g], v[b, g], causal,
+                                                           scale, lo, hi)
+    return O, L
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,102 @@
+"""A block of Nq queries against an Nk-row key/value cache (decoding), split
+over the keys, through the C ABI (attn_fwd_kv) and the merge, against the
+fp64 oracle (attention_kv).
+
+Partials: |O_s - O_s,ref| <= 2e-2, |LSE_s - LSE_s,ref| <= 5e-3 where the
+split sees a key, LSE_s = -inf exactly where it sees none; merged result
+against the oracle's whole-cache attention at the same tolerances.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import to64
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, LSE_TOL = 2e-2, 5e-3
+
+
+def _check(attn, q, k, v, causal, n_split, scale):
+    Op, Lp = attn.fwd_kv(q.cuda(), k.cuda(), v.cuda(), n_split, causal=causal, scale=scale)
+    O, L = attn.merge(Op, Lp)
+    assert attn.poll_status() == (0, 0)
+    q64, k64, v64 = to64(q), to64(k), to64(v)
+    O_ref_p, L_ref_p = oracle.attention_kv(q64, k64, v64, causal, scale, n_split)
+    Lp64 = to64(Lp)
+    assert np.array_equal(np.isneginf(Lp64), np.isneginf(L_ref_p))
+    seen = ~np.isneginf(L_ref_p)
+    assert np.max(np.abs(Lp64[seen] - L_ref_p[seen]), initial=0.0) <= LSE_TOL
+    assert np.max(np.abs(to64(Op) - O_ref_p)) <= O_TOL
+    O_ref, L_ref = oracle.attention_kv(q64, k64, v64, causal, scale, 1)
+    assert np.max(np.abs(to64(O) - O_ref[0])) <= O_TOL
+    assert np.max(np.abs(to64(L) - L_ref[0])) <= LSE_TOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,dtype,n_split", [
+    (1, 4, 2, 1, 1000, 128, "bf16", 1),
+    (1, 4, 2, 1, 1000, 128, "bf16", 4),
+    (2, 2, 2, 7, 300, 64, "fp16", 2),
+    (1, 6, 3, 128, 513, 96, "bf16", 3),
+    (1, 2, 1, 129, 129, 128, "bf16", 1),
+    (1, 2, 2, 200, 777, 128, "fp16", 5),
+    (1, 1, 1, 1, 1, 64, "bf16", 1),
+    (1, 2, 1, 3, 257, 96, "fp16", 8),
+])
+def test_queries_against_a_cache(attn_lib, causal, B, Hq, Hkv, Nq, Nk, d, dtype, n_split):
+    w = wl.Workload("kv", "fwd", B, Hq, Nk, d, dtype, causal, seed=Nq + Nk + d)
+    inp = wl.make_inputs(w)
+    # the queries are the cache's last Nq positions of the seeded q; the
+    # key/value heads the first head of each group
+    G = Hq // Hkv
+    q = inp["q"][:, :, Nk - Nq:].contiguous()
+    k, v = inp["k"][:, ::G].contiguous(), inp["v"][:, ::G].contiguous()
+    _check(attn_lib, q, k, v, causal, n_split, w.scale)
+
+
+def test_equal_lengths_match_the_split_forward_bitwise(attn_lib):
+    w = wl.Workload("kv", "fwd", 1, 2, 700, 128, "bf16", True, seed=5)
+    inp = wl.make_inputs(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    a = attn_lib.fwd_kv(q, k, v, 3, causal=True)
+    b = attn_lib.fwd_split(q, k, v, 3, causal=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_decode_workload_sampled_heads(attn_lib):
+    """The measured decode batch (one query per sequence against an 8192-row
+    cache, 16 sequences x 16 heads, d = 128, bf16, 4 splits + merge) in the
+    launch configuration the bench times; eight (sequence, head) pairs,
+    the first and the last among them, against the oracle."""
+    w = wl.DECODE_BF16_D128
+    inp = wl.make_decode_inputs(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    Op, Lp = attn_lib.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal, scale=w.scale)
+    O, L = attn_lib.merge(Op, Lp)
+    assert attn_lib.poll_status() == (0, 0)
+    for b, h in [(0, 0), (0, 15), (3, 7), (7, 1), (9, 12), (12, 4), (15, 8), (15, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        q64, k64, v64 = (to64(inp[n][sl]) for n in ("q", "k", "v"))
+        O_ref_p, L_ref_p = oracle.attention_kv(q64, k64, v64, w.causal, w.scale,
+                                               wl.DECODE_SPLITS)
+        assert np.max(np.abs(to64(Op[:, b, h]) - O_ref_p[:, 0, 0])) <= O_TOL
+        assert np.max(np.abs(to64(Lp[:, b, h]) - L_ref_p[:, 0, 0])) <= LSE_TOL
+        O_ref, L_ref = oracle.attention_kv(q64, k64, v64, w.causal, w.scale, 1)
+        assert np.max(np.abs(to64(O[b, h]) - O_ref[0, 0, 0])) <= O_TOL
+        assert np.max(np.abs(to64(L[b, h]) - L_ref[0, 0, 0])) <= LSE_TOL
+
+
+def test_more_queries_than_keys_is_rejected(attn_lib):
+    L = attn_lib.lib()
+    x = torch.zeros((1, 1, 256, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 256), dtype=torch.float32, device="cuda")
+    p, pl = ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(lse.data_ptr())
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # Nq = 200 > Nk = 100: ATTN_ERR_INVALID_ARG before any launch
+    assert L.attn_fwd_kv(p, p, p, p, pl, 1, 1, 1, 1, 200, 100, 64, 1, 0.125, 1, s) == 1
+    assert attn_lib.poll_status() == (0, 0)

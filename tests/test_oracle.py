@@ -596,3 +596,56 @@ def test_dq_rows_equal_the_full_backward(causal):
     rows = [0, 1, 17, 36]
     assert np.allclose(oracle.attention_backward_dq_rows(q, k, v, do, rows, causal, 0.45),
                        dQ[rows], rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------- queries against a cache ---
+
+@pytest.mark.parametrize("nq,nk", [(1, 9), (3, 9), (5, 5), (4, 130)])
+def test_kv_queries_are_the_suffix_of_full_causal_attention(nq, nk):
+    """The Nq queries are the last Nq positions: their rows of the full
+    causal attention over all Nk positions (top-left, pinned above) are the
+    key-cache attention with the bottom-right offset."""
+    d, scale = 6, 0.37
+    q_full, k, v = _rand(nk, d), _rand(nk, d), _rand(nk, d)
+    O_full, L_full, _ = oracle.attention_head(q_full, k, v, True, scale)
+    O, L = oracle.attention_kv_head(q_full[nk - nq:], k, v, True, scale)
+    assert np.allclose(O, O_full[nk - nq:], atol=1e-12, rtol=0)
+    assert np.allclose(L, L_full[nk - nq:], atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_head_brute_force(causal):
+    nq, nk, d, scale = 3, 7, 4, 0.5
+    q, k, v = _rand(nq, d), _rand(nk, d), _rand(nk, d)
+    O, L = oracle.attention_kv_head(q, k, v, causal, scale)
+    for i in range(nq):
+        keys = [j for j in range(nk) if not causal or j <= nk - nq + i]
+        s = [scale * sum(q[i, c] * k[j, c] for c in range(d)) for j in keys]
+        m = max(s)
+        tot = sum(math.exp(x - m) for x in s)
+        assert abs(L[i] - (m + math.log(tot))) < 1e-12
+        for c in range(d):
+            o = sum(math.exp(x - m) / tot * v[j, c] for x, j in zip(s, keys))
+            assert abs(O[i, c] - o) < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_split_merges_to_the_whole_and_matches_split_at_equal_lengths(causal):
+    B, Hq, Hkv, nq, nk, d, scale = 1, 4, 2, 3, 300, 5, 0.3
+    q, k, v = _rand(B, Hq, nq, d), _rand(B, Hkv, nk, d), _rand(B, Hkv, nk, d)
+    Op, Lp = oracle.attention_kv(q, k, v, causal, scale, n_split=4)
+    O1, L1 = oracle.attention_kv(q, k, v, causal, scale, n_split=1)
+    O, L = oracle.merge_partials(Op, Lp)
+    assert np.allclose(O, O1[0], atol=1e-12) and np.allclose(L, L1[0], atol=1e-12)
+    # grouped heads = attention with each key/value head repeated per group
+    rep = np.repeat(k, Hq // Hkv, axis=1), np.repeat(v, Hq // Hkv, axis=1)
+    O2, L2 = oracle.attention_kv(q, *rep, causal, scale, n_split=4)
+    assert np.allclose(O2, Op, atol=1e-12) and np.array_equal(np.isneginf(L2), np.isneginf(Lp))
+    # Nq = Nk: the key-cache attention is attention_split
+    qn = _rand(B, Hkv, nk, d)
+    Os, Ls = oracle.attention_split(qn, k, v, causal, scale, 3)
+    Ok, Lk = oracle.attention_kv(qn, k, v, causal, scale, n_split=3)
+    assert np.allclose(Os, Ok, atol=1e-12)
+    assert np.array_equal(np.isneginf(Ls), np.isneginf(Lk))
+    fin = ~np.isneginf(Ls)
+    assert np.allclose(Ls[fin], Lk[fin], atol=1e-12)

@@ -84,6 +84,14 @@ FWD_FP8_D128 = Workload("fwd_fp8_causal_b2h16n8192d128", "fwd_fp8", 2, 16, 8192,
 
 WORKLOADS = [TINY_FWD_FP16, FWD_FP16_D64, FWD_BF16_D128, BWD_BF16_D128, FWD_FP8_D128]
 
+# Decoding against a key/value cache (split over the keys, then merged): one
+# new query per sequence, 16 sequences x 16 heads, an 8192-row cache of the
+# bf16 d=128 workload's head size.  N is the cache length.
+DECODE_BF16_D128 = Workload("decode_bf16_b16h16nk8192d128", "fwd_kv", 16, 16, 8192, 128, "bf16",
+                            True)
+DECODE_NQ = 1
+DECODE_SPLITS = 4
+
 
 def sweep_d64(causal: bool) -> List[Workload]:
     """fp16 d=64 forward at N in {512..8192}, B = 16384 / N, H = 16."""
@@ -162,6 +170,17 @@ def make_varlen_inputs(lengths: List[int], Hq: int, Hkv: int, d: int, dtype: str
         cu.append(cu[-1] + int(n))
     out["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32)
     return out
+
+
+def make_decode_inputs(w: Workload, nq: int = DECODE_NQ) -> Dict[str, torch.Tensor]:
+    """Inputs of a decode step on the CPU: q [B,H,nq,d], k, v [B,H,N,d] (N the
+    cache length), fp32 standard normals drawn in the order q, k, v and cast
+    to the workload's dtype."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.B, w.H, nq, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32)
+    return {n: t.to(w.torch_dtype) for n, t in (("q", q), ("k", k), ("v", v))}
 
 
 def head_range(rank: int, world: int, BH: int) -> range:
