@@ -454,39 +454,46 @@ def decode_timing(attn, dev, stream, peaks, iters=20):
     """Decoding against a key/value cache, timed apart from the step: one
     query per sequence, 16 sequences x 16 heads, an 8192-row bf16 d=128
     cache, split over the keys into 4 runs (attn_fwd_kv) and merged
-    (attn_merge).  HBM-bound: the algorithmic bytes are the cache's K and V
+    (attn_merge); and the same with 2 key/value heads.  HBM-bound: the algorithmic bytes are the cache's K and V
     read once (plus q, the partials and O, under 0.1 %).  Inputs are seeded
     standard normals drawn on the device (timing only; parity is in the
     tests); L2 is flushed before every call."""
     w = wl.DECODE_BF16_D128
-    g = torch.Generator(device=dev).manual_seed(0)
-    q = torch.randn((w.B, w.H, wl.DECODE_NQ, w.d), generator=g, device=dev).to(torch.bfloat16)
-    k, v = (torch.randn((w.B, w.H, w.N, w.d), generator=g, device=dev).to(torch.bfloat16)
-            for _ in range(2))
-    Op, Lp = attn.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal)
-    O, L = attn.merge(Op, Lp)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    n_split = wl.DECODE_SPLITS
+    for hkv in (w.H, wl.DECODE_GQA_KV_HEADS):
+        g = torch.Generator(device=dev).manual_seed(0)
+        q = torch.randn((w.B, w.H, wl.DECODE_NQ, w.d), generator=g, device=dev) \
+            .to(torch.bfloat16)
+        k, v = (torch.randn((w.B, hkv, w.N, w.d), generator=g, device=dev).to(torch.bfloat16)
+                for _ in range(2))
+        Op, Lp = attn.fwd_kv(q, k, v, n_split, causal=w.causal)
+        O, L = attn.merge(Op, Lp)
 
-    def step():
-        attn.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal, out=Op, lse=Lp)
-        attn.merge(Op, Lp, out=O, lse=L)
+        def step():
+            attn.fwd_kv(q, k, v, n_split, causal=w.causal, out=Op, lse=Lp)
+            attn.merge(Op, Lp, out=O, lse=L)
 
-    ts = _timed(step, stream, flush, iters)
-    status = attn.poll_status()
-    if status[0] != 0:
-        raise RuntimeError(f"device status after the decode timing: {status}")
-    r = _summary(ts)
-    kv_bytes = 2 * w.B * w.H * w.N * w.d * 2
-    gbs = kv_bytes / (r["ms_median"] * 1e-3) / 1e9
-    r.update({"workload": w.name, "n_split": wl.DECODE_SPLITS, "queries": wl.DECODE_NQ,
-              "gbs": round(gbs, 1),
-              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                           "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                           "algorithmic_bytes": kv_bytes},
-              "note": "fwd_kv (4 key splits) + merge, L2 flushed, timed apart from the step "
-                      "(not in value)"})
-    del q, k, v, Op, Lp, O, L
-    return r
+        ts = _timed(step, stream, flush, iters)
+        status = attn.poll_status()
+        if status[0] != 0:
+            raise RuntimeError(f"device status after the decode timing: {status}")
+        r = _summary(ts)
+        kv_bytes = 2 * w.B * hkv * w.N * w.d * 2
+        gbs = kv_bytes / (r["ms_median"] * 1e-3) / 1e9
+        r.update({"workload": w.name, "kv_heads": hkv, "n_split": n_split,
+                  "queries": wl.DECODE_NQ, "gbs": round(gbs, 1),
+                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": round(gbs / peaks["hbm_gbs"], 4),
+                               "algorithmic_bytes": kv_bytes}})
+        out["mha" if hkv == w.H else "gqa"] = r
+        del q, k, v, Op, Lp, O, L
+    out["note"] = ("fwd_kv (key splits) + merge, L2 flushed, timed apart from the step "
+                   "(not in value); gqa: 16 query heads on 2 key/value heads, a group's "
+                   "8 queries in one tile")
+    return out
 
 
 def varlen_timing(attn, dev, stream, iters=10):

@@ -156,6 +156,7 @@ attn_status fill_fwd_common(FwdLaunch* a, DeviceInfo* di, int B, int H, int N, f
   p.BH = B * H;
   p.N = N;
   p.Nk = N;
+  p.q_zrows = N;
   p.n_qtiles = (N + 127) / 128;
   p.n_pairs = (p.n_qtiles + 1) / 2;
   p.n_kblocks = (N + 127) / 128;
@@ -214,13 +215,23 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
   // tensor-map head index: (batch, head) for dense tensors, head for packed ones
   const int64_t zq = varlen ? H : BH, zkv = varlen ? Hkv : BHkv;
-  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, zq, 64, 128) ||
+  // Grouped heads whose queries fit one tile together (decoding: few
+  // queries per head) share it: Q / O are then viewed as [B, H * N, d].
+  const bool pack = !varlen && Hkv < H && (int64_t)(H / Hkv) * N <= 128;
+  const int64_t q_rows = pack ? (int64_t)H * N : N, q_z = pack ? B : zq;
+  if (!encode_3d(&a.tmQ, q, dt, 2, d, q_rows, q_z, 64, 128) ||
       !encode_3d(&a.tmK, k, dt, 2, d, Nk, zkv, 64, 128) ||
       !encode_3d(&a.tmV, v, dt, 2, d, Nk, zkv, 64, 128))
     return ATTN_ERR_CUDA;
   fill_fwd_common(&a, di, B, H, N, scale, stream, o, lse);
   FwdParams& p = a.params;
   p.Nk = Nk;
+  if (pack) {
+    p.pack_nq = N;
+    p.q_zrows = H * N;
+    p.n_pairs = 1;
+    p.num_units = B * Hkv;  // one unit per (batch, key/value head)
+  }
   p.n_kblocks = (Nk + 127) / 128;
   p.heads_kv = Hkv;
   p.group = H / Hkv;

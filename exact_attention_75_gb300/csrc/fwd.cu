@@ -76,7 +76,8 @@ struct Unit {
   int bh, qp;
   int bhkv;   // key/value head (batch * heads_kv + head / group)
   int zq, zkv;  // tensor-map head index of Q / O and of K / V
-  int row0;   // first row of the sequence in its head
+  int row0;   // first row of the sequence in its head (K / V)
+  int qrow;   // tensor-map row of the unit's first query row (Q / O)
   int len;    // query rows of the sequence
   int klen;   // key rows of the sequence
   int koff;   // causal: query row i sees keys j <= i + koff
@@ -91,6 +92,29 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   Unit w;
   w.split = u % p.n_split;  // splits of one query-tile pair are neighbours
   u /= p.n_split;
+  if (p.pack_nq > 0) {
+    // Grouped heads packed into tile 0: u = (batch, key/value head).
+    const int b = u / p.heads_kv;
+    const int g = u - b * p.heads_kv;
+    w.bh = b * p.heads + g * p.group;
+    w.qp = 0;
+    w.bhkv = u;
+    w.zkv = u;
+    w.zq = b;
+    w.row0 = 0;
+    w.qrow = g * p.group * p.pack_nq;
+    w.len = p.group * p.pack_nq;
+    w.klen = p.Nk;
+    w.koff = p.Nk - p.pack_nq;
+    w.nkb = (w.klen + 127) >> 7;
+    w.kb0 = (w.split * w.nkb) / p.n_split;
+    const int kb1 = ((w.split + 1) * w.nkb) / p.n_split;
+    // causal: the last query of a head sees keys up to pack_nq - 1 + koff
+    const int visible = CAUSAL ? min((p.pack_nq - 1 + w.koff) / 128 + 1, w.nkb) : w.nkb;
+    w.nb[0] = max(0, min(visible, kb1) - w.kb0);
+    w.nb[1] = 0;
+    return w;
+  }
   if (CAUSAL || p.cu_seqlens != nullptr) {
     // Longest first: the heaviest query-tile pairs of every head come first.
     const int r = u / p.BH;
@@ -107,6 +131,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     const int s0 = min(max(__ldg(p.cu_seqlens + b), 0), p.N);
     const int s1 = min(max(__ldg(p.cu_seqlens + b + 1), s0), p.N);
     w.row0 = s0;
+    w.qrow = s0;
     w.len = min(s1 - s0, p.max_seqlen);
     w.klen = w.len;
     w.koff = 0;
@@ -115,6 +140,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     w.bhkv = w.zkv;
   } else {
     w.row0 = 0;
+    w.qrow = 0;
     w.len = p.N;
     w.klen = p.Nk;
     w.koff = p.Nk - p.N;
@@ -205,12 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
           const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
           if constexpr (FP8) {
-            tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, w.row0 + (2 * w.qp + t) * 128, w.zq);
+            tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, w.qrow + (2 * w.qp + t) * 128, w.zq);
           } else {
 #pragma unroll
             for (int h = 0; h < kPaddedD<D> / 64; ++h)
               tma_load_3d(dst + h * 16384, &tmQ, bar(L::kQFull + t), h * 64,
-                          w.row0 + (2 * w.qp + t) * 128, w.zq);
+                          w.qrow + (2 * w.qp + t) * 128, w.zq);
           }
           ++q_it[t];
         }
@@ -448,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nb == 0) {
         // A query tile that sees no key of this split: O = 0, LSE = -inf.
         if (row < w.len) {
-          const size_t grow = (size_t)w.zq * p.N + w.row0 + row;
+          const size_t grow = (size_t)w.zq * p.q_zrows + w.qrow + row;
           uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -511,7 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool tail = (jk == w.nkb - 1) && (w.klen & 127);
         if (diag || tail) {
           const int kbase = jk * 128;
-          const int lim = CAUSAL ? min(row + w.koff, w.klen - 1) : (w.klen - 1);
+          // query index within its head (packed heads: pack_nq rows each)
+          const int qi = p.pack_nq > 0 ? r % p.pack_nq : row;
+          const int lim = CAUSAL ? min(qi + w.koff, w.klen - 1) : (w.klen - 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
@@ -622,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A row that sees no key of this split (a short query block against a
       // longer cache) has l = 0: O = 0, LSE = -inf.
       const float inv_l = l > 0.f ? (FP8 ? sv_max : 1.0f) / l : 0.f;
-      const size_t grow = (size_t)w.zq * p.N + w.row0 + row;
+      const size_t grow = (size_t)w.zq * p.q_zrows + w.qrow + row;
       uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

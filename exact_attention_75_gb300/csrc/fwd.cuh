@@ -16,6 +16,15 @@ struct FwdParams {
   // attends to a longer key cache).  Causal masking is aligned at the
   // bottom right: query row i sits at key position i + Nk - N.
   int Nk;
+  // Rows per tensor-map head index of the Q / O layout (N; heads * N when
+  // grouped heads are packed).
+  int q_zrows;
+  // Grouped query heads packed into one tile (pack_nq = N > 0, dense only,
+  // group * N <= 128): a work unit is (batch, key/value head, split) and its
+  // single query tile holds the group's query heads, N rows each, contiguous
+  // in the [B, heads * N, D] view of Q and O.  Each K/V block is then read and
+  // multiplied once per group instead of once per query head.
+  int pack_nq = 0;
   int n_qtiles;         // ceil(N / 128)
   int n_pairs;          // ceil(n_qtiles / 2): work units per head
   int n_kblocks;        // ceil(N / 128)

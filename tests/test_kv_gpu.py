@@ -47,6 +47,10 @@ def _check(attn, q, k, v, causal, n_split, scale):
     (1, 2, 2, 200, 777, 128, "fp16", 5),
     (1, 1, 1, 1, 1, 64, "bf16", 1),
     (1, 2, 1, 3, 257, 96, "fp16", 8),
+    (2, 8, 2, 5, 300, 128, "bf16", 3),     # 4 heads x 5 queries share a tile
+    (1, 16, 1, 8, 1000, 64, "fp16", 2),    # 16 x 8 = 128 rows: a full shared tile
+    (1, 9, 3, 40, 700, 96, "bf16", 1),     # 3 x 40 = 120 rows
+    (1, 8, 2, 20, 20, 128, "bf16", 1),     # Nq = Nk, shared tile, causal top-left
 ])
 def test_queries_against_a_cache(attn_lib, causal, B, Hq, Hkv, Nq, Nk, d, dtype, n_split):
     w = wl.Workload("kv", "fwd", B, Hq, Nk, d, dtype, causal, seed=Nq + Nk + d)
@@ -68,20 +72,25 @@ def test_equal_lengths_match_the_split_forward_bitwise(attn_lib):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_decode_workload_sampled_heads(attn_lib):
-    """The measured decode batch (one query per sequence against an 8192-row
-    cache, 16 sequences x 16 heads, d = 128, bf16, 4 splits + merge) in the
-    launch configuration the bench times; eight (sequence, head) pairs,
-    the first and the last among them, against the oracle."""
+@pytest.mark.parametrize("kv_heads", [16, wl.DECODE_GQA_KV_HEADS])
+def test_decode_workload_sampled_heads(attn_lib, kv_heads):
+    """The measured decode batches (one query per sequence against an
+    8192-row cache, 16 sequences x 16 query heads with 16 or 2 key/value
+    heads, d = 128, bf16, 4 splits + merge; with 2 the 8 query heads of a
+    group share one query tile) in the launch configuration the bench times;
+    eight (sequence, head) pairs, the first and the last among them, against
+    the oracle."""
     w = wl.DECODE_BF16_D128
-    inp = wl.make_decode_inputs(w)
+    inp = wl.make_decode_inputs(w, kv_heads=kv_heads)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
     Op, Lp = attn_lib.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal, scale=w.scale)
     O, L = attn_lib.merge(Op, Lp)
     assert attn_lib.poll_status() == (0, 0)
+    G = w.H // kv_heads
     for b, h in [(0, 0), (0, 15), (3, 7), (7, 1), (9, 12), (12, 4), (15, 8), (15, 15)]:
         sl = (slice(b, b + 1), slice(h, h + 1))
-        q64, k64, v64 = (to64(inp[n][sl]) for n in ("q", "k", "v"))
+        q64 = to64(inp["q"][sl])
+        k64, v64 = (to64(inp[n][b:b + 1, h // G:h // G + 1]) for n in ("k", "v"))
         O_ref_p, L_ref_p = oracle.attention_kv(q64, k64, v64, w.causal, w.scale,
                                                wl.DECODE_SPLITS)
         assert np.max(np.abs(to64(Op[:, b, h]) - O_ref_p[:, 0, 0])) <= O_TOL

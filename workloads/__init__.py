@@ -91,6 +91,9 @@ DECODE_BF16_D128 = Workload("decode_bf16_b16h16nk8192d128", "fwd_kv", 16, 16, 81
                             True)
 DECODE_NQ = 1
 DECODE_SPLITS = 4
+# The same batch with grouped heads: 16 query heads sharing 2 key/value heads
+# (a group's 8 queries share one query tile).
+DECODE_GQA_KV_HEADS = 2
 
 
 def sweep_d64(causal: bool) -> List[Workload]:
@@ -172,14 +175,16 @@ def make_varlen_inputs(lengths: List[int], Hq: int, Hkv: int, d: int, dtype: str
     return out
 
 
-def make_decode_inputs(w: Workload, nq: int = DECODE_NQ) -> Dict[str, torch.Tensor]:
-    """Inputs of a decode step on the CPU: q [B,H,nq,d], k, v [B,H,N,d] (N the
-    cache length), fp32 standard normals drawn in the order q, k, v and cast
-    to the workload's dtype."""
+def make_decode_inputs(w: Workload, nq: int = DECODE_NQ,
+                       kv_heads: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Inputs of a decode step on the CPU: q [B,H,nq,d], k, v [B,Hkv,N,d] (N the
+    cache length, Hkv = kv_heads or H), fp32 standard normals drawn in the
+    order q, k, v and cast to the workload's dtype."""
+    hkv = w.H if kv_heads is None else kv_heads
     g = torch.Generator().manual_seed(w.seed)
     q = torch.randn((w.B, w.H, nq, w.d), generator=g, dtype=torch.float32)
-    k = torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32)
-    v = torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, hkv, w.N, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, hkv, w.N, w.d), generator=g, dtype=torch.float32)
     return {n: t.to(w.torch_dtype) for n, t in (("q", q), ("k", k), ("v", v))}
 
 
