@@ -53,6 +53,11 @@ constexpr int kWarpRelay = 10;
 // Named barriers (0 is __syncthreads): issuer <-> relay, issuer <-> softmax t.
 constexpr uint32_t kBarKv = 1, kBarP = 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+// How work units map to rows (a compile-time choice, so each kernel carries
+// only its own unit decoding): dense [B*H, N, D] heads; grouped heads packed
+// into one query tile (FwdParams::pack_nq); packed variable-length batches
+// (FwdParams::cu_seqlens).
+constexpr int kModeDense = 0, kModePacked = 1, kModeVarlen = 2;
 constexpr int kPrecF16 = 0, kPrecBF16 = 1, kPrecE4M3 = 2;
 
 template <int D, bool FP8>
@@ -87,35 +92,42 @@ struct Unit {
   int nb[2];  // K/V blocks visited by query tile 0 / 1 (0: tile absent or no key in the split)
 };
 
+// Grouped heads packed into one query tile: u = (batch, key/value head, split).
 template <bool CAUSAL>
+__device__ __forceinline__ Unit decode_packed_unit(int u, const FwdParams& p) {
+  Unit w;
+  w.split = u % p.n_split;
+  u /= p.n_split;
+  const int b = u / p.heads_kv;
+  const int g = u - b * p.heads_kv;
+  w.bh = b * p.heads + g * p.group;
+  w.qp = 0;
+  w.bhkv = u;
+  w.zkv = u;
+  w.zq = b;
+  w.row0 = 0;
+  w.qrow = g * p.group * p.pack_nq;
+  w.len = p.group * p.pack_nq;
+  w.klen = p.Nk;
+  w.koff = p.Nk - p.pack_nq;
+  w.nkb = (w.klen + 127) >> 7;
+  w.kb0 = (w.split * w.nkb) / p.n_split;
+  const int kb1 = ((w.split + 1) * w.nkb) / p.n_split;
+  // causal: the last query of a head sees keys up to pack_nq - 1 + koff
+  const int visible = CAUSAL ? min((p.pack_nq - 1 + w.koff) / 128 + 1, w.nkb) : w.nkb;
+  w.nb[0] = max(0, min(visible, kb1) - w.kb0);
+  w.nb[1] = 0;
+  return w;
+}
+
+template <bool CAUSAL, int MODE>
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
+  if constexpr (MODE == kModePacked) return decode_packed_unit<CAUSAL>(u, p);
+  constexpr bool VARLEN = MODE == kModeVarlen;
   Unit w;
   w.split = u % p.n_split;  // splits of one query-tile pair are neighbours
   u /= p.n_split;
-  if (p.pack_nq > 0) {
-    // Grouped heads packed into tile 0: u = (batch, key/value head).
-    const int b = u / p.heads_kv;
-    const int g = u - b * p.heads_kv;
-    w.bh = b * p.heads + g * p.group;
-    w.qp = 0;
-    w.bhkv = u;
-    w.zkv = u;
-    w.zq = b;
-    w.row0 = 0;
-    w.qrow = g * p.group * p.pack_nq;
-    w.len = p.group * p.pack_nq;
-    w.klen = p.Nk;
-    w.koff = p.Nk - p.pack_nq;
-    w.nkb = (w.klen + 127) >> 7;
-    w.kb0 = (w.split * w.nkb) / p.n_split;
-    const int kb1 = ((w.split + 1) * w.nkb) / p.n_split;
-    // causal: the last query of a head sees keys up to pack_nq - 1 + koff
-    const int visible = CAUSAL ? min((p.pack_nq - 1 + w.koff) / 128 + 1, w.nkb) : w.nkb;
-    w.nb[0] = max(0, min(visible, kb1) - w.kb0);
-    w.nb[1] = 0;
-    return w;
-  }
-  if (CAUSAL || p.cu_seqlens != nullptr) {
+  if (CAUSAL || VARLEN) {
     // Longest first: the heaviest query-tile pairs of every head come first.
     const int r = u / p.BH;
     w.bh = u - r * p.BH;
@@ -126,7 +138,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   }
   const int b = w.bh / p.heads;
   const int hq = w.bh - b * p.heads;
-  if (p.cu_seqlens != nullptr) {
+  if constexpr (VARLEN) {
     // rows clamped into [0, N] so that no access leaves the tensors
     const int s0 = min(max(__ldg(p.cu_seqlens + b), 0), p.N);
     const int s1 = min(max(__ldg(p.cu_seqlens + b + 1), s0), p.N);
@@ -165,7 +177,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   return w;
 }
 
-template <int D, bool CAUSAL, int PREC>
+template <int D, bool CAUSAL, int PREC, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -222,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok; ++k) {
         const int u = snake_unit(k, cta, G);
         if (u >= p.num_units) break;
-        const Unit w = decode_unit<CAUSAL>(u, p);
+        const Unit w = decode_unit<CAUSAL, MODE>(u, p);
         if (max(w.nb[0], w.nb[1]) == 0) continue;  // no key of the split is visible
         for (int t = 0; t < 2 && ok; ++t) {
           if (w.nb[t] == 0) continue;
@@ -231,12 +243,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
           const uint32_t dst = sbase + L::kQOff + t * L::kTileBytes;
           if constexpr (FP8) {
-            tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, w.qrow + (2 * w.qp + t) * 128, w.zq);
+            tma_load_3d(dst, &tmQ, bar(L::kQFull + t), 0, w.row0 + (2 * w.qp + t) * 128, w.zq);
           } else {
 #pragma unroll
             for (int h = 0; h < kPaddedD<D> / 64; ++h)
               tma_load_3d(dst + h * 16384, &tmQ, bar(L::kQFull + t), h * 64,
-                          w.qrow + (2 * w.qp + t) * 128, w.zq);
+                          (MODE == kModePacked ? w.qrow : w.row0) + (2 * w.qp + t) * 128, w.zq);
           }
           ++q_it[t];
         }
@@ -299,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0;; ++k) {
       const int u = snake_unit(k, cta, G);
       if (u >= p.num_units) break;
-      const Unit w = decode_unit<CAUSAL>(u, p);
+      const Unit w = decode_unit<CAUSAL, MODE>(u, p);
       const int nbmax = max(w.nb[0], w.nb[1]);
       if (nbmax == 0) continue;  // the same skip in every role
 #pragma unroll
@@ -371,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0;; ++k) {
       const int u = snake_unit(k, cta, G);
       if (u >= p.num_units) break;
-      const Unit w = decode_unit<CAUSAL>(u, p);
+      const Unit w = decode_unit<CAUSAL, MODE>(u, p);
       const int nb0 = w.nb[0], nb1 = w.nb[1];
       const int nbmax = max(nb0, nb1);
       if (nbmax == 0) continue;  // the same skip in every role
@@ -464,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0;; ++k) {
       const int u = snake_unit(k, cta, G);
       if (u >= p.num_units) break;
-      const Unit w = decode_unit<CAUSAL>(u, p);
+      const Unit w = decode_unit<CAUSAL, MODE>(u, p);
       const int nb = w.nb[t];
       const int tile = 2 * w.qp + t;
       const int row = tile * 128 + r;
@@ -474,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nb == 0) {
         // A query tile that sees no key of this split: O = 0, LSE = -inf.
         if (row < w.len) {
-          const size_t grow = (size_t)w.zq * p.q_zrows + w.qrow + row;
+          const size_t grow = MODE == kModePacked ? (size_t)w.zq * p.q_zrows + w.qrow + row
+                                : (size_t)w.zq * p.N + w.row0 + row;
           uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -538,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (diag || tail) {
           const int kbase = jk * 128;
           // query index within its head (packed heads: pack_nq rows each)
-          const int qi = p.pack_nq > 0 ? r % p.pack_nq : row;
+          const int qi = MODE == kModePacked ? r % p.pack_nq : row;
           const int lim = CAUSAL ? min(qi + w.koff, w.klen - 1) : (w.klen - 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
@@ -650,7 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A row that sees no key of this split (a short query block against a
       // longer cache) has l = 0: O = 0, LSE = -inf.
       const float inv_l = l > 0.f ? (FP8 ? sv_max : 1.0f) / l : 0.f;
-      const size_t grow = (size_t)w.zq * p.q_zrows + w.qrow + row;
+      const size_t grow = MODE == kModePacked ? (size_t)w.zq * p.q_zrows + w.qrow + row
+                                : (size_t)w.zq * p.N + w.row0 + row;
       uint4* orow = reinterpret_cast<uint4*>(obase + grow * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -682,11 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, int PREC>
+template <int D, bool CAUSAL, int PREC, int MODE>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& params, int num_ctas, cudaStream_t stream) {
   using L = FwdLayout<D, PREC == kPrecE4M3>;
-  auto kern = fwd_kernel<D, CAUSAL, PREC>;
+  auto kern = fwd_kernel<D, CAUSAL, PREC, MODE>;
   static bool configured = false;  // attribute set once per instantiation
   if (!configured) {
     cudaError_t e =
@@ -702,8 +716,16 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 template <int D, int PREC>
 cudaError_t launch_dc(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                       const FwdParams& p, int n, cudaStream_t s, bool causal) {
-  return causal ? launch_one<D, true, PREC>(q, k, v, p, n, s)
-                : launch_one<D, false, PREC>(q, k, v, p, n, s);
+  if constexpr (PREC != kPrecE4M3) {
+    if (p.pack_nq > 0)
+      return causal ? launch_one<D, true, PREC, kModePacked>(q, k, v, p, n, s)
+                    : launch_one<D, false, PREC, kModePacked>(q, k, v, p, n, s);
+    if (p.cu_seqlens != nullptr)
+      return causal ? launch_one<D, true, PREC, kModeVarlen>(q, k, v, p, n, s)
+                    : launch_one<D, false, PREC, kModeVarlen>(q, k, v, p, n, s);
+  }
+  return causal ? launch_one<D, true, PREC, kModeDense>(q, k, v, p, n, s)
+                : launch_one<D, false, PREC, kModeDense>(q, k, v, p, n, s);
 }
 
 }  // namespace
