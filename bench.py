@@ -444,7 +444,7 @@ def tensor_peaks(dev, stream, iters=20):
         ts = _timed(lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one,
                                              out_dtype=torch.bfloat16), stream, flush, iters)
         res["e4m3_tflops"] = round(2 * M ** 3 / (statistics.median(ts) * 1e-3) / 1e12, 1)
-    except Exception as e:  # the library may not offer the product on this build
+    except Exception as e:  # the installed library may not offer the E4M3 product
         res["e4m3_unavailable"] = str(e).splitlines()[0][:200]
     res["note"] = "8192^3, median of 20 launches, L2 flushed; burst"
     return res
@@ -669,7 +669,6 @@ def cpu_oracle_sample(budget_s: float = 20.0):
     Forward + backward of one (b, h) head at N = 8192, d = 128; repeated while
     the time budget lasts.  Returns (TFLOP/s, seconds, heads done, threads).
     """
-    import numpy as np
     import oracle
     w = WORKLOAD.with_(B=1, H=1)
     inp = wl.make_inputs(w, with_do=True)
@@ -684,7 +683,6 @@ def cpu_oracle_sample(budget_s: float = 20.0):
             break
     dt = time.perf_counter() - t0
     fl = heads * (w.fwd_flops() + w.bwd_flops())
-    _ = np
     return fl / dt / 1e12, dt, heads, os.cpu_count()
 
 
