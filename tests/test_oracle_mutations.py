@@ -45,6 +45,14 @@ MUTATIONS = {
         "s = np.float32(amax) / np.float32(E4M3_MAX) if amax > 0 else np.float32(1.0)",
         "s = np.float32(amax) / np.float32(240.0) if amax > 0 else np.float32(1.0)"),
     "Hadamard sign": ("H = np.block([[H, H], [H, -H]])", "H = np.block([[H, H], [-H, H]])"),
+    "sequences end one row early": ("return list(zip(cu[:-1], cu[1:]))",
+                                    "return list(zip(cu[:-1], [c - 1 for c in cu[1:]]))"),
+    "sequence keys from the query head": (
+        "attention_head(q[h, lo:hi], k[g, lo:hi], v[g, lo:hi],",
+        "attention_head(q[h, lo:hi], k[h % np.shape(k)[0], lo:hi], v[g, lo:hi],"),
+    "rotation signs on the wrong side": ("return hadamard_matrix(d) * s[None, :] / math.sqrt(d)",
+                                         "return hadamard_matrix(d) * s[:, None] / math.sqrt(d)"),
+    "rotation transposed": ("x = x @ rotation_matrix(signs)", "x = x @ rotation_matrix(signs).T"),
 }
 
 
@@ -182,8 +190,41 @@ def check_hadamard(m):
         assert np.all(H[0] == 1) and np.all(H[:, 0] == 1)  # Sylvester order
 
 
+def check_varlen(m):
+    r = _rng()
+    lens = [3, 0, 5, 2]
+    cu = np.cumsum([0] + lens)
+    T, d, Hq, Hkv = int(cu[-1]), 3, 4, 2
+    q = r.standard_normal((Hq, T, d))
+    k, v = r.standard_normal((Hkv, T, d)), r.standard_normal((Hkv, T, d))
+    O, L = m["attention_varlen"](q, k, v, cu, True, 0.5)
+    for lo, hi in zip(cu[:-1], cu[1:]):
+        if hi == lo:
+            continue
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            Ob, Lb = _brute_rows(q[h, lo:hi], k[g, lo:hi], v[g, lo:hi], 0.5, lambda i, j: j <= i)
+            assert np.allclose(O[h, lo:hi], Ob, atol=1e-12)
+            assert np.allclose(L[h, lo:hi], Lb, atol=1e-12)
+
+
+def check_rotation(m):
+    """R = H_d diag(signs) / sqrt(d) built here from scalar loops; the
+    quantizer rotates rows as x R."""
+    d = 8
+    signs = np.array([1, -1, -1, 1, 1, 1, -1, 1], np.float64)
+
+    def h(i, j):  # Sylvester entry: (-1)^popcount(i & j)
+        return -1.0 if bin(i & j).count("1") % 2 else 1.0
+    R = np.array([[h(i, j) * signs[j] / math.sqrt(d) for j in range(d)] for i in range(d)])
+    assert np.allclose(m["rotation_matrix"](signs), R, atol=1e-15)
+    x = _rng().standard_normal((1, 1, 4, d))
+    out = m["quantize_blocks"](x, 64, signs)
+    assert np.array_equal(out["x32"], (x @ R).astype(np.float32))
+
+
 CHECKS = [check_forward, check_backward, check_key_cache, check_split_and_merge,
-          check_grouped_heads, check_quantize, check_hadamard]
+          check_grouped_heads, check_varlen, check_quantize, check_hadamard, check_rotation]
 
 
 def _failures(m):
