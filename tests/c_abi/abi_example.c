@@ -2,7 +2,9 @@
  * The C ABI used from plain C (no Python): a causal fp16 forward pass of one
  * head, [1,1,N,64], on the default stream.  Causal query row 0 sees only key
  * 0, so its output row equals V's row 0 and its LSE equals scale * q0 . k0;
- * the program checks both and that every output is finite, then prints OK.
+ * the program checks both and that every output is finite; decoding the last
+ * position with attn_fwd_kv (one query against the whole sequence as a
+ * key/value cache) must give the last output row and LSE; then it prints OK.
  * Build: cc -std=c99 -I include abi_example.c -L <dir of libattn.so> -lattn
  *        -L <cuda>/lib64 -lcudart -lm
  */
@@ -86,6 +88,24 @@ int main(void) {
     if (!isfinite(from_half(o[i]))) ++bad;
   for (int i = 0; i < N; ++i)
     if (!isfinite(lse[i])) ++bad;
+  /* Decoding the last position against the whole sequence as a key/value
+   * cache (Nq = 1, Nk = N, causal) gives the forward's last row. */
+  void* o1_d = NULL;
+  float* lse1_d = NULL;
+  if (cudaMalloc(&o1_d, D * 2) != 0 || cudaMalloc((void**)&lse1_d, 16) != 0) return 2;
+  const uint16_t* q_last = (const uint16_t*)dev[0] + (size_t)(N - 1) * D;
+  st = attn_fwd_kv(q_last, dev[1], dev[2], o1_d, lse1_d, 1, 1, 1, 1, 1, N, D, 1, scale,
+                   ATTN_F16, NULL);
+  if (st != ATTN_OK) ++bad;
+  uint16_t o1[D];
+  float lse1 = 0.f;
+  if (cudaMemcpy(o1, o1_d, sizeof(o1), D2H) != 0) return 2;
+  if (cudaMemcpy(&lse1, lse1_d, sizeof(lse1), D2H) != 0) return 2;
+  for (int c = 0; c < D; ++c)
+    if (fabs(from_half(o1[c]) - from_half(o[(size_t)(N - 1) * D + c])) > 1e-2) ++bad;
+  if (fabs(lse1 - lse[N - 1]) > 1e-3) ++bad;
+  cudaFree(o1_d);
+  cudaFree(lse1_d);
   /* an invalid argument is rejected before any launch */
   if (attn_fwd(dev[0], dev[1], dev[2], dev[3], lse_d, 1, 1, N, 80, 1, scale, ATTN_F16, NULL) ==
       ATTN_OK)
