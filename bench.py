@@ -162,6 +162,105 @@ def max_over_ranks(values):
     return [float(x) for x in t.cpu()]
 
 
+class CudaTimer:
+    """Device timing on one stream with CUDA events."""
+
+    def __init__(self, stream):
+        self.stream = stream
+
+    def sync(self):
+        torch.cuda.synchronize()
+
+    def mark(self):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        return e
+
+    def elapsed_ms(self, a, b):
+        return a.elapsed_time(b)
+
+
+def timed_region(steps, run_step, world, timer, on_start=None):
+    """Time exactly `steps` calls of run_step: every rank meets at a barrier,
+    the device is synchronised, the steps run between two timer marks, the
+    device is synchronised again and the ranks meet once more.  Returns this
+    rank's elapsed milliseconds."""
+    if world > 1:
+        torch.distributed.barrier()
+    timer.sync()
+    if on_start is not None:
+        on_start()
+    t0 = timer.mark()
+    for _ in range(steps):
+        run_step()
+    t1 = timer.mark()
+    timer.sync()
+    if world > 1:
+        torch.distributed.barrier()
+    return timer.elapsed_ms(t0, t1)
+
+
+def job_times(ms_step, e2e_ms, world):
+    """Per-step times of the whole job: the slowest rank's."""
+    if world > 1:
+        ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
+    return ms_step, e2e_ms
+
+
+def job_value(step_flops, ms, world):
+    """Whole-job TFLOP/s: every rank processes its own batch of step_flops
+    (weak scaling) in the slowest rank's time ms."""
+    return world * step_flops / (ms * 1e-3) / 1e12
+
+
+def component_roofline(c, flops, nbytes, ms, peaks):
+    """Roofline object of one component of the step: tensor-bound
+    contractions against the measured dense bf16 peak (the E4M3 forward
+    against twice that, the nominal FP8:bf16 ratio, as no FP8 peak is
+    measured by the driver), the quantization pass against HBM bandwidth."""
+    if flops > 0:
+        ach = flops / (ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * (2 if c == "fwd_fp8" else 1)
+        kind = f"{peaks['source']} bf16 burst" + (" x2 (nominal E4M3 ratio)" if c == "fwd_fp8"
+                                                   else "")
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": measured_traffic(c),
+                "algorithmic_bytes": nbytes, "peak_kind": kind}
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(c),
+            "algorithmic_bytes": nbytes, "peak_kind": f"{peaks['source']} HBM copy"}
+
+
+def rank_env(gpus):
+    """(rank, world, local_rank) from torchrun's environment (1 rank
+    without it); --gpus must match the launched world size."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != gpus:
+        raise SystemExit(f"bench.py: --gpus {gpus} but {world} rank(s) were launched "
+                         f"(WORLD_SIZE={os.environ.get('WORLD_SIZE')})")
+    return int(os.environ.get("RANK", "0")), world, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def launch_ranks_if_needed(args):
+    """--gpus N > 1 run as a plain process: launch N ranks (one per GPU of
+    this node) through torch.distributed.run on 127.0.0.1 with the same
+    arguments, wait for them and return True.  Under torchrun: False."""
+    if args.gpus <= 1 or "WORLD_SIZE" in os.environ:
+        return False
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    rc = subprocess.call(cmd)
+    if rc != 0:
+        raise SystemExit(rc)
+    return True
+
+
 def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
     """Weak scaling: rank r owns global heads [r*B*H, (r+1)*B*H) of a job of
     world*B*H independent heads; its slice is drawn with seed r."""
@@ -248,11 +347,6 @@ def component_bytes(w: wl.Workload):
             "bwd": 8 * elems * 2 + BH * N * 4,
             "quant": 3 * (elems * 2 + elems + BH * ((N + 63) // 64) * 4),
             "fwd_fp8": 3 * elems + elems * 2 + BH * N * 4 + 3 * BH * ((N + 63) // 64) * 4}
-
-
-def available_components(attn, step_probe=None):
-    """The components of one step (every one is always run)."""
-    return list(COMPONENTS)
 
 
 SPLIT_KV_N = 4  # key splits of the split-KV measurement
@@ -538,18 +632,9 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = WORKLOAD
-    comps = []
-    # keep only components the library implements (unsupported ones raise)
-    trial = Step(attn, w.with_(B=1, H=1, N=256), dev, COMPONENTS)
-    for c in available_components(attn):
-        try:
-            trial.run(c)
-            torch.cuda.synchronize()
-            comps.append(c)
-        except Exception as e:  # noqa: BLE001
-            if "UNSUPPORTED" not in str(e):
-                raise
-    del trial
+    # Every component of the step runs; one the library rejects (for instance
+    # with ATTN_ERR_UNSUPPORTED) fails the bench instead of shrinking the step.
+    comps = list(COMPONENTS)
     st = Step(attn, rank_workload(w, rank), dev, comps)
     flops = component_flops(w)
     nbytes = component_bytes(w)
@@ -564,15 +649,8 @@ def run_gpu(args, rank, world, local_rank):
 
     ev = {c: [] for c in comps}
     sampler = ClockSampler(local_rank)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
+
+    def one_step():
         for c in comps:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -580,12 +658,10 @@ def run_gpu(args, rank, world, local_rank):
             st.run(c)
             e1.record(stream)
             ev[c].append((e0, e1))
-    t1.record(stream)
-    torch.cuda.synchronize()
+
+    ms_total = timed_region(args.steps, one_step, world, CudaTimer(stream),
+                            on_start=lambda: (sampler.start(), time.sleep(0.3)))
     clocks = sampler.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    ms_total = t0.elapsed_time(t1)
     per = {c: statistics.mean(a.elapsed_time(b) for a, b in ev[c]) for c in comps}
     status = attn.poll_status()
     if status[0] != 0:
@@ -652,9 +728,7 @@ def run_gpu(args, rank, world, local_rank):
     decode = decode_timing(attn, dev, stream, load_peaks())
 
     step_flops = sum(flops[c] for c in comps)
-    ms_step = ms_total / args.steps
-    if world > 1:
-        ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms])
+    ms_step, e2e_ms = job_times(ms_total / args.steps, e2e_ms, world)
     return dict(comps=comps, per=per, ms_step=ms_step, e2e_ms=e2e_ms, clocks=clocks, split=split,
                 gqa=gqa, varlen=varlen, head_dims=head_dims, decode=decode,
                 flops=flops, nbytes=nbytes, step_flops=step_flops, h2d=h2d, d2h=d2h,
@@ -700,9 +774,9 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if launch_ranks_if_needed(args):
+        return
+    rank, world, local_rank = rank_env(args.gpus)
     peaks = load_peaks()
     w = WORKLOAD
 
@@ -763,33 +837,31 @@ def main():
         return
 
     comps, per = r["comps"], r["per"]
-    value = world * r["step_flops"] / (r["ms_step"] * 1e-3) / 1e12
-    e2e_val = world * r["step_flops"] / (r["e2e_ms"] * 1e-3) / 1e12
+    value = job_value(r["step_flops"], r["ms_step"], world)
+    e2e_val = job_value(r["step_flops"], r["e2e_ms"], world)
     breakdown = {}
     for c in comps:
         ms = per[c]
         tf = r["flops"][c] / (ms * 1e-3) / 1e12 if r["flops"][c] else None
         breakdown[c] = {"ms": round(ms, 4), "tflops": None if tf is None else round(tf, 1),
-                        "gbs": round(r["nbytes"][c] / (ms * 1e-3) / 1e9, 1)}
+                        "gbs": round(r["nbytes"][c] / (ms * 1e-3) / 1e9, 1),
+                        "roofline": component_roofline(c, r["flops"][c], r["nbytes"][c], ms,
+                                                       peaks)}
     # dominant kernel = largest share of the step's time
     dom = max(comps, key=lambda c: per[c])
-    if r["flops"][dom] > 0:
-        ach = r["flops"][dom] / (per[dom] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        if dom == "fwd_fp8":
-            peak = 2 * peaks["bf16_tflops"]  # E4M3 dense = 2x bf16 (nominal ratio)
-        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": measured_traffic(dom),
-                "peak_kind": f"{peaks['source']} bf16 burst"}
-    else:
-        ach = r["nbytes"][dom] / (per[dom] * 1e-3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": measured_traffic(dom)}
+    roof = dict(breakdown[dom]["roofline"], kernel=dom)
+    # the 16-bit part of the step alone (the E4M3 forward computes in FP8)
+    bf16_comps = [c for c in ("fwd", "bwd") if c in comps]
+    bf16_value = job_value(sum(r["flops"][c] for c in bf16_comps),
+                           sum(per[c] for c in bf16_comps), world)
     line = {"metric": "attention fwd/bwd TFLOP/s", "value": round(value, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(r["ms_step"], 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16+e4m3",
+            "dtype_note": "value counts the bf16 forward and backward and the E4M3 forward "
+                          "(the quantization pass counts no FLOPs); value_bf16 is the bf16 "
+                          "forward + backward alone",
+            "value_bf16": round(bf16_value, 2), "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "causal": w.causal, "components": comps,
                        "l2": "inputs (q,k,v,dO = 256 MiB) larger than L2; no flush",

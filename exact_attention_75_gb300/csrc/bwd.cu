@@ -42,6 +42,7 @@
 
 #include "bwd.cuh"
 #include "sm103_ptx.cuh"
+#include "smem_attr.cuh"
 #include "tiles.cuh"
 
 namespace attn {
@@ -1109,13 +1110,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 }
 
 template <typename Kern>
-cudaError_t launch_persistent(Kern kern, int threads, int bytes, bool* configured,
+cudaError_t launch_persistent(Kern kern, int threads, int bytes, DeviceFlags& configured,
                               const BwdLaunch& a, int units) {
-  if (!*configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    *configured = true;
-  }
+  cudaError_t e = ensure_dyn_smem(kern, bytes, configured);
+  if (e != cudaSuccess) return e;
   const int grid = units < a.num_sms ? units : a.num_sms;
   kern<<<grid, threads, bytes, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmDO, a.params);
   return cudaGetLastError();
@@ -1123,13 +1121,13 @@ cudaError_t launch_persistent(Kern kern, int threads, int bytes, bool* configure
 
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_main(const BwdLaunch& a) {
-  static bool dkv_configured = false, dq_configured = false;
+  static DeviceFlags dkv_configured, dq_configured;  // per device and instantiation
   cudaError_t e = launch_persistent(bwd_dkv_kernel<D, CAUSAL, BF16>, kThreads,
-                                    DkvLayout<D>::kBytes, &dkv_configured, a,
+                                    DkvLayout<D>::kBytes, dkv_configured, a,
                                     a.params.BHkv * a.params.n_kblocks);
   if (e != cudaSuccess) return e;
   return launch_persistent(bwd_dq_kernel<D, CAUSAL, BF16>, kThreads, DqLayout<D>::kBytes,
-                           &dq_configured, a, a.params.BH * a.params.n_qtiles);
+                           dq_configured, a, a.params.BH * a.params.n_qtiles);
 }
 
 template <int D, bool BF16>

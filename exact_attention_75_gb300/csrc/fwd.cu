@@ -40,6 +40,7 @@
 #include "fp8.cuh"
 #include "fwd.cuh"
 #include "sm103_ptx.cuh"
+#include "smem_attr.cuh"
 #include "tiles.cuh"
 
 namespace attn {
@@ -701,13 +702,9 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
                        const FwdParams& params, int num_ctas, cudaStream_t stream) {
   using L = FwdLayout<D, PREC == kPrecE4M3>;
   auto kern = fwd_kernel<D, CAUSAL, PREC, MODE>;
-  static bool configured = false;  // attribute set once per instantiation
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static DeviceFlags configured;  // attribute set once per device and instantiation
+  cudaError_t e = ensure_dyn_smem(kern, L::kDynSmem, configured);
+  if (e != cudaSuccess) return e;
   const int grid = params.num_units < num_ctas ? params.num_units : num_ctas;
   kern<<<grid, kThreads, L::kDynSmem, stream>>>(tmQ, tmK, tmV, params);
   return cudaGetLastError();

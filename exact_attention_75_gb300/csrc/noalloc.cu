@@ -1,16 +1,17 @@
 // attn_bwd_noalloc: the backward pass for callers that cannot allocate
 // device memory.
 //
-// attn_bwd needs a caller-provided workspace (the fp32 delta vector).  Some callers cannot provide one: code running inside a
-// host framework whose allocator owns all device memory and hands plugins no
-// raw allocations, real-time serving loops where a cudaMalloc (which may
-// synchronise the device) is not allowed on the request path, or embedded
-// users with a fixed memory plan.  For them this file keeps the workspace in a
-// file-scope device array of fixed size, so the call itself allocates nothing.
+// attn_bwd needs a caller-provided workspace (the fp32 delta vector).  Some
+// callers cannot provide one: code running inside a host framework whose
+// allocator owns all device memory and hands plugins no raw allocations,
+// real-time serving loops where a cudaMalloc (which may synchronise the
+// device) is not allowed on the request path, or embedded users with a fixed
+// memory plan.  For them this file keeps the workspace in a file-scope device
+// array of fixed size, so the call itself allocates nothing.
 //
-// The array holds kMaxRows query rows of scratch: it is part
-// of the library image and occupies that much memory on every GPU that loads
-// the library, until the process exits.  All calls share it.
+// The array holds kMaxRows query rows of scratch: it is part of the library
+// image and occupies that much memory on every GPU that loads the library,
+// until the process exits.  All calls share it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -59,9 +60,9 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
   void* scratch = nullptr;
   const attn_status st = scratch_address(&scratch);
   if (st != ATTN_OK) return st;
-  // attn_bwd writes delta before reading it and zeroes the dQ accumulator on
-  // the stream before accumulating, so leftovers of the previous call in the
-  // shared array do not matter.
+  // The array holds only the delta vector D.  attn_bwd's D pass writes
+  // delta[row] for every row < B*H*N on this stream before either main
+  // kernel reads it, so leftovers of an earlier call are never read.
   return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, kScratchBytes, B, H, N, d, causal,
                   scale, dtype, stream);
 }

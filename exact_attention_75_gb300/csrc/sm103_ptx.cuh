@@ -69,14 +69,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The clock is read after every failed try_wait (each one suspends the thread
+// for a hardware-defined time at most), so even a limit of a microsecond is
+// honoured; the CTA's abort flag (a shared-memory load) every 8 attempts.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, Watchdog wd,
                                             uint32_t where) {
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*wd.abort_flag) return false;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 7) == 0 && *wd.abort_flag) return false;
     if (globaltimer_ns() - t0 > wd.limit_ns) {
       report_failure(wd, where);
       return false;

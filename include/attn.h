@@ -246,7 +246,9 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
  *   them) race on it.
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress) with that device current; make that
- *   first call before any stream capture.
+ *   first call before any stream capture.  The address is kept for the
+ *   life of the process: calls made after cudaDeviceReset on that device
+ *   are not supported (the array may then sit elsewhere).
  */
 attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                              const void* dout, const float* lse, void* dq, void* dk, void* dv,

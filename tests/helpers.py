@@ -1,4 +1,7 @@
 """Shared helpers for the GPU parity tests (not collected by pytest)."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -21,3 +24,15 @@ def sample_heads(B: int, H: int, n: int, seed: int):
     while len(heads) < min(n, B * H):
         heads.add((int(g.integers(0, B)), int(g.integers(0, H))))
     return sorted(heads)
+
+
+def record(name: str, values: dict) -> None:
+    """Write measured values (errors, ratios) of a test to
+    $ATTN_RECORD_DIR/<name>.json when that variable is set; a no-op
+    otherwise.  The records are measurements, never expected values."""
+    out = os.environ.get("ATTN_RECORD_DIR")
+    if not out:
+        return
+    os.makedirs(out, exist_ok=True)
+    with open(os.path.join(out, f"{name}.json"), "w") as f:
+        json.dump(values, f, indent=1, sort_keys=True)

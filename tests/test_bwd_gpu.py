@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads as wl
-from helpers import sample_heads, to64
+from helpers import sample_heads, sample_rows, to64
 
 pytestmark = pytest.mark.gpu
 REL_TOL = 5e-2
@@ -61,22 +61,46 @@ def test_small_shapes_full(attn_lib, dtype, causal, B, H, N, d):
     _check(w, grads, refs)
 
 
+def _check_sampled_head(inp, grads, b, h, causal, scale, seed, n_rows=48):
+    """One head of a workload too large for the full oracle: dQ on seeded
+    sampled rows (the oracle computes each row's dQ on its own), and dK, dV
+    through identities that hold at any size (every row of dS sums to zero,
+    so the sum of dK over the keys vanishes; every row of P sums to one, so
+    the sum of dV over the keys equals the sum of dO over the queries)."""
+    N = inp["q"].shape[2]
+    qh, kh, vh, doh = (to64(inp[n][b, h]) for n in ("q", "k", "v", "do"))
+    rows = sample_rows(N, n_rows, seed=seed)
+    dq_ref = oracle.attention_backward_dq_rows(qh, kh, vh, doh, rows, causal, scale)
+    dq = to64(grads[0][b, h])
+    assert np.max(np.abs(dq[rows] - dq_ref)) <= REL_TOL * np.max(np.abs(dq_ref)), (b, h)
+    dkh, dvh = to64(grads[1][b, h]), to64(grads[2][b, h])
+    assert np.all(np.abs(dkh.sum(axis=0)) <= 1e-2 * np.abs(dkh).sum(axis=0)), (b, h)
+    assert np.all(np.abs(dvh.sum(axis=0) - doh.sum(axis=0)) <= 1e-2 * np.abs(dvh).sum(axis=0))
+
+
 def test_bf16_backward_workload(attn_lib):
-    """[2,16,8192,128] bf16 causal; the oracle recomputes two whole heads."""
+    """[2,16,8192,128] bf16 causal on four seeded heads including the first
+    and the last: the oracle recomputes those two heads whole; the other two
+    are checked on sampled dQ rows and the dK / dV sum identities."""
     w = wl.BWD_BF16_D128
     inp = wl.make_inputs(w)
     grads = _gpu_grads(attn_lib, inp, w)
-    heads = [(0, 0), (1, 15)]
+    heads = sample_heads(w.B, w.H, 4, seed=4)
+    full = [(0, 0), (w.B - 1, w.H - 1)]
+    assert len(heads) == 4 and all(hd in heads for hd in full)
     refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), True,
-                                     w.scale, heads=heads)
-    _check(w, grads, refs, heads)
+                                     w.scale, heads=full)
+    _check(w, grads, refs, full)
+    for (b, h) in heads:
+        if (b, h) not in full:
+            _check_sampled_head(inp, grads, b, h, True, w.scale, seed=b * 131 + h)
 
 
 def test_noncausal_medium(attn_lib):
     w = wl.Workload("bwd_nc", "bwd", 1, 4, 2048, 128, "bf16", False, seed=3)
     inp = wl.make_inputs(w)
     grads = _gpu_grads(attn_lib, inp, w)
-    heads = sample_heads(1, 4, 2, seed=1)
+    heads = sample_heads(1, 4, 4, seed=1)
     refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), False,
                                      w.scale, heads=heads)
     _check(w, grads, refs, heads)

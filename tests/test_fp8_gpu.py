@@ -6,18 +6,21 @@ On inputs with 0.1% x20 outliers the prescribed quantization by itself
 (evaluated in fp64 by the oracle, no kernel involved) already exceeds that
 bound, so there the kernel's own error is measured against the
 quantization-aware oracle (fp64 attention on the oracle's dequantized,
-rotated inputs) with the same 3e-2 bound, and its total error must stay
-within 0.01 of the recipe's floor."""
+rotated inputs) with the same 3e-2 bound, and its total error against the
+exact oracle may exceed the recipe's own floor (the fp64 emulation of the
+quantization, no kernel involved) by at most 25 % on the small cases and
+10 % on the full-size workload (measured on a GB300: at most 1.17x and 1.03x)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads as wl
-from helpers import sample_heads, sample_rows, to64
+from helpers import record, sample_heads, sample_rows, to64
 
 pytestmark = pytest.mark.gpu
 RMSE_TOL = 3e-2
+FLOOR_RATIO_SMALL, FLOOR_RATIO_WORKLOAD = 1.25, 1.10
 
 
 def _quant(attn, x, signs=None, transposed=False):
@@ -134,7 +137,7 @@ def test_fp8_forward_outlier_inputs(attn_lib, hadamard, causal, N):
     """0.1% x20 outliers.  The prescribed quantization alone (fp64 emulation,
     no kernel involved) already costs about 0.04 RMSE here, so the kernel is
     held to (a) RMSE <= 3e-2 against the quantization-aware fp64 oracle (its
-    own error) and (b) RMSE against the exact oracle within 0.01 of that
+    own error) and (b) RMSE against the exact oracle at most 1.25x that
     emulated floor."""
     w = wl.Workload("f8o", "fwd_fp8", 1, 3, N, 128, "bf16", causal, outliers=True,
                     hadamard=hadamard, seed=N + 1)
@@ -145,15 +148,17 @@ def test_fp8_forward_outlier_inputs(attn_lib, hadamard, causal, N):
     O_ref, _ = oracle.attention(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), causal, w.scale)
     O_qa, L_qa = oracle.attention(*_quant_aware_inputs(inp, hadamard), causal, w.scale)
     floor = oracle.rmse(O_qa, O_ref)
+    record(f"fp8_outliers_n{N}_c{int(causal)}_h{int(hadamard)}",
+           {"e_exact": oracle.rmse(O, O_ref), "e_floor": floor, "e_kern": oracle.rmse(O, O_qa)})
     assert oracle.rmse(O, O_qa) <= RMSE_TOL
-    assert oracle.rmse(O, O_ref) <= floor + 0.01, (oracle.rmse(O, O_ref), floor)
+    assert oracle.rmse(O, O_ref) <= FLOOR_RATIO_SMALL * floor, (oracle.rmse(O, O_ref), floor)
     assert np.max(np.abs(to64(lse) - L_qa)) < 0.05
 
 
 def test_fp8_forward_workload(attn_lib):
     """[2,16,8192,128] causal, 0.1% x20 outliers, Hadamard on Q and K: on
     seeded sampled rows of four heads, RMSE against the quantization-aware
-    oracle <= 3e-2 and against the exact oracle within 0.01 of the floor."""
+    oracle <= 3e-2 and against the exact oracle at most 1.1x the floor."""
     w = wl.FWD_FP8_D128
     inp = wl.make_inputs(w)
     o, _ = _fp8_forward(attn_lib, inp, w)
@@ -177,8 +182,11 @@ def test_fp8_forward_workload(attn_lib):
     e_kern, e_exact, e_floor = rm(d_kern), rm(d_exact), rm(d_floor)
     print(f"FP8 workload RMSE: vs exact {e_exact:.4f}, recipe floor {e_floor:.4f}, "
           f"kernel own {e_kern:.4f}")
+    record("fp8_workload_rmse", {"e_exact": e_exact, "e_floor": e_floor, "e_kern": e_kern,
+                                 "ratio_exact_to_floor": e_exact / e_floor,
+                                 "rows": "64 seeded rows of 4 heads, (0,0) and (1,15) included"})
     assert e_kern <= RMSE_TOL
-    assert e_exact <= e_floor + 0.01
+    assert e_exact <= FLOOR_RATIO_WORKLOAD * e_floor, (e_exact, e_floor)
     _ = signs
 
 
@@ -196,4 +204,6 @@ def test_fp8_block_scaling_and_rotation_reduce_error(attn_lib):
     e_blk, e_pt = oracle.rmse(to64(o_blk), O_ref), oracle.rmse(to64(o_pt), O_ref)
     print(f"FP8 RMSE per-tensor {e_pt:.3e}  per-block+Hadamard {e_blk:.3e}  "
           f"ratio {e_pt / e_blk:.2f}")
+    record("fp8_scaling_ratio", {"rmse_per_tensor": e_pt, "rmse_per_block_hadamard": e_blk,
+                                 "ratio": e_pt / e_blk, "shape": [1, 4, 2048, 128]})
     assert e_blk < e_pt

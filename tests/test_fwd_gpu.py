@@ -102,13 +102,13 @@ def test_bf16_d128_workload(attn_lib, causal):
 @pytest.mark.parametrize("causal", [True, False])
 def test_d64_sweep(attn_lib, causal):
     for w in wl.sweep_d64(causal):
-        _sampled_compare(attn_lib, w, n_heads=2, n_rows=16)
+        _sampled_compare(attn_lib, w, n_heads=4, n_rows=16)
 
 
 @pytest.mark.parametrize("causal", [True, False])
 def test_d128_sweep(attn_lib, causal):
     for w in wl.sweep_d128(causal):
-        _sampled_compare(attn_lib, w, n_heads=2, n_rows=16)
+        _sampled_compare(attn_lib, w, n_heads=4, n_rows=16)
 
 
 def test_q_zero_causal_prefix_mean_at_full_size(attn_lib):
