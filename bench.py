@@ -423,20 +423,26 @@ def gqa_timing(attn, st, w, stream, hkv, iters=10):
             "note": "grouped query heads, timed apart from the step (not in value)"}
 
 
+HEAD_DIMS = (64, 96, 192, 256)   # timed beside the step's d = 128
+WIDE_BACKWARD = False            # the backward at d in {192, 256}
+
+
 def head_dim_timing(attn, w, dev, stream, iters=10):
-    """Forward + backward at the other head dims (64 and 96) on the step's
-    B, H, N, dtype and masking, timed apart from the step.  Inputs are
-    standard normals drawn on the device from a seeded generator (timing
-    only; parity at these head dims is in the tests)."""
+    """Forward + backward at the other head dims on the step's B, H, N,
+    dtype and masking, timed apart from the step.  Inputs are standard
+    normals drawn on the device from a seeded generator (timing only; parity
+    at these head dims is in the tests)."""
     out = {}
     g = torch.Generator(device=dev).manual_seed(1234)
-    for d in (64, 96):
+    for d in HEAD_DIMS:
+        with_bwd = d <= 128 or WIDE_BACKWARD
         wd = w.with_(d=d)
         shape = (wd.B, wd.H, wd.N, d)
         q, k, v, do = (torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
                        .to(torch.bfloat16) for _ in range(4))
         o, lse = attn.fwd(q, k, v, causal=wd.causal, scale=wd.scale)
-        grads = attn.bwd(q, k, v, o, do, lse, causal=wd.causal, scale=wd.scale)
+        grads = attn.bwd(q, k, v, o, do, lse, causal=wd.causal, scale=wd.scale) \
+            if with_bwd else None
         torch.cuda.synchronize()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         tf, tb = [], []
@@ -444,8 +450,9 @@ def head_dim_timing(attn, w, dev, stream, iters=10):
             e[0].record(stream)
             attn.fwd(q, k, v, causal=wd.causal, scale=wd.scale, out=o, lse=lse)
             e[1].record(stream)
-            attn.bwd(q, k, v, o, do, lse, causal=wd.causal, scale=wd.scale, dq=grads[0],
-                     dk=grads[1], dv=grads[2])
+            if with_bwd:
+                attn.bwd(q, k, v, o, do, lse, causal=wd.causal, scale=wd.scale, dq=grads[0],
+                         dk=grads[1], dv=grads[2])
             e[2].record(stream)
             torch.cuda.synchronize()
             tf.append(e[0].elapsed_time(e[1]))
@@ -454,9 +461,14 @@ def head_dim_timing(attn, w, dev, stream, iters=10):
         if status[0] != 0:
             raise RuntimeError(f"device status after the d={d} timing: {status}")
         mf, mb = statistics.mean(tf), statistics.mean(tb)
-        out[f"d{d}"] = {"fwd_ms": round(mf, 4), "bwd_ms": round(mb, 4),
-                        "fwd_tflops": round(wd.fwd_flops() / (mf * 1e-3) / 1e12, 1),
-                        "bwd_tflops": round(wd.bwd_flops() / (mb * 1e-3) / 1e12, 1)}
+        pk = load_peaks()["bf16_tflops"]
+        r = {"fwd_ms": round(mf, 4), "fwd_tflops": round(wd.fwd_flops() / (mf * 1e-3) / 1e12, 1)}
+        r["fwd_frac"] = round(r["fwd_tflops"] / pk, 4)
+        if with_bwd:
+            r.update({"bwd_ms": round(mb, 4),
+                      "bwd_tflops": round(wd.bwd_flops() / (mb * 1e-3) / 1e12, 1)})
+            r["bwd_frac"] = round(r["bwd_tflops"] / pk, 4)
+        out[f"d{d}"] = r
         del q, k, v, do, o, lse, grads
     out["note"] = "bf16, the step's B, H, N and masking; timed apart from the step (not in value)"
     return out

@@ -137,9 +137,11 @@ cudaError_t launch_varlen_check(const int* cu, int n_seq, int total, int max_seq
   return cudaGetLastError();
 }
 
+bool head_dim_ok(int d) { return d == 64 || d == 96 || d == 128 || d == 192 || d == 256; }
+
 bool shape_ok(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return false;
-  if (d != 64 && d != 96 && d != 128) return false;
+  if (!head_dim_ok(d)) return false;
   const int64_t bh = (int64_t)B * H;
   if (bh > (1 << 30) || N > (1 << 28)) return false;
   return bh * N * d < (int64_t)1 << 40;
@@ -202,10 +204,14 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   if (Nk == 0) Nk = N;
   if (Nk < N || (varlen && Nk != N) || !shape_ok(B, Hkv, Nk, d)) return ATTN_ERR_INVALID_ARG;
+  // The wide head dims run one query tile per unit, dense or grouped heads
+  // only: no key split, key cache or packed variable-length batch.
+  const bool wide = d > 128;
+  if (wide && (n_split != 1 || varlen || Nk != N)) return ATTN_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
   if (st != ATTN_OK) return st;
@@ -217,7 +223,7 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   const int64_t zq = varlen ? H : BH, zkv = varlen ? Hkv : BHkv;
   // Grouped heads whose queries fit one tile together (decoding: few
   // queries per head) share it: Q / O are then viewed as [B, H * N, d].
-  const bool pack = !varlen && Hkv < H && (int64_t)(H / Hkv) * N <= 128;
+  const bool pack = !wide && !varlen && Hkv < H && (int64_t)(H / Hkv) * N <= 128;
   const int64_t q_rows = pack ? (int64_t)H * N : N, q_z = pack ? B : zq;
   if (!encode_3d(&a.tmQ, q, dt, 2, d, q_rows, q_z, 64, 128) ||
       !encode_3d(&a.tmK, k, dt, 2, d, Nk, zkv, 64, 128) ||
@@ -252,6 +258,10 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   p.num_units *= n_split;
   p.o_split = (size_t)BH * N * d;
   p.lse_split = (size_t)BH * N;
+  if (wide) {
+    p.num_units = p.BH * p.n_qtiles;  // one query tile per unit
+    return launch_result(launch_fwd_wide(a, d, causal != 0, dtype == ATTN_BF16));
+  }
   cudaError_t e = launch_fwd(a, d, causal != 0, dtype == ATTN_BF16);
   return launch_result(e);
 }

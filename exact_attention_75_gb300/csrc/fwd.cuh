@@ -61,5 +61,8 @@ struct FwdLaunch {
 };
 
 cudaError_t launch_fwd(const FwdLaunch& a, int d, bool causal, bool bf16);
+// d in {192, 256}: one query tile per work unit (fwd_wide.cu); dense or
+// grouped heads, no key split, no packed or variable-length modes.
+cudaError_t launch_fwd_wide(const FwdLaunch& a, int d, bool causal, bool bf16);
 
 }  // namespace attn
