@@ -424,7 +424,7 @@ def gqa_timing(attn, st, w, stream, hkv, iters=10):
 
 
 HEAD_DIMS = (64, 96, 192, 256)   # timed beside the step's d = 128
-WIDE_BACKWARD = False            # the backward at d in {192, 256}
+WIDE_BACKWARD = True             # the backward at d in {192, 256}
 
 
 def head_dim_timing(attn, w, dev, stream, iters=10):

@@ -134,7 +134,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
         lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """O, LSE = attention(q, k, v).  q: [B,H,N,d], k, v: [B,Hkv,N,d] (Hkv
-    divides H; fewer heads = grouped query heads) fp16/bf16, d in {64,96,128}."""
+    divides H; fewer heads = grouped query heads) fp16/bf16, d in {64,96,128,192,256}."""
     if k.dim() == 4 and q.dim() == 4 and k.shape[1] != q.shape[1]:
         return _fwd_gqa(q, k, v, causal, scale, out, lse)
     B, H, N, d = _check_qkv(q, k, v)
@@ -258,7 +258,7 @@ def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def bwd(q, k, v, o, do, lse, causal: bool = False, scale: Optional[float] = None,
         workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None):
-    """dQ, dK, dV of the loss with gradient ``do`` w.r.t. O (d in {64, 96, 128}).  k, v
+    """dQ, dK, dV of the loss with gradient ``do`` w.r.t. O (d in {64, 96, 128, 192, 256}).  k, v
     (and dk, dv) may have fewer heads than q (grouped query heads)."""
     B, H, N, d = _check_qkv(q, o, do)
     Hkv = _check_kv_heads(q, k, v)

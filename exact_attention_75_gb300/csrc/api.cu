@@ -356,6 +356,57 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
 
 namespace {
 
+// The backward pass at d in {192, 256} (arguments already checked): the D
+// pass, then the dK/dV kernel (Q and dO read 64 rows at a time) and the dQ
+// kernel (K and V read 64 rows at a time).
+attn_status bwd_wide_impl(DeviceInfo* di, const void* q, const void* k, const void* v,
+                          const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                          void* dv, void* workspace, int B, int H, int Hkv, int N, int d,
+                          int causal, float scale, attn_dtype dtype, void* stream) {
+  BwdWideLaunch a;
+  const CUtensorMapDataType dt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
+  if (!encode_3d(&a.tmQ, q, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmK, k, dt, 2, d, N, BHkv, 64, 128) ||
+      !encode_3d(&a.tmV, v, dt, 2, d, N, BHkv, 64, 128) ||
+      !encode_3d(&a.tmDO, dout, dt, 2, d, N, BH, 64, 128) ||
+      !encode_3d(&a.tmQ64, q, dt, 2, d, N, BH, 64, 64) ||
+      !encode_3d(&a.tmK64, k, dt, 2, d, N, BHkv, 64, 64) ||
+      !encode_3d(&a.tmV64, v, dt, 2, d, N, BHkv, 64, 64) ||
+      !encode_3d(&a.tmDO64, dout, dt, 2, d, N, BH, 64, 64))
+    return ATTN_ERR_CUDA;
+  BwdParams& p = a.params;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.delta = static_cast<float*>(workspace);
+  p.status = di->status;
+  p.BH = (int)BH;
+  p.BHkv = (int)BHkv;
+  p.heads = H;
+  p.heads_kv = Hkv;
+  p.group = H / Hkv;
+  p.N = N;
+  p.n_qtiles = (N + 127) / 128;
+  p.n_kblocks = (N + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  a.num_sms = di->num_sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.causal = causal != 0;
+  a.bf16 = dtype == ATTN_BF16;
+  a.d = d;
+  return launch_result(launch_bwd_wide(a));
+}
+
 // The backward pass; with cu_seqlens the packed variable-length layout of
 // fwd_impl (dq like q, dk / dv like k / v).
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
@@ -375,13 +426,18 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
+  // the wide head dims: dense or grouped heads only
+  if (d > 128 && varlen) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(varlen ? 1 : B, H, N, d))
     return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
   if (st != ATTN_OK) return st;
+  if (d > 128)
+    return bwd_wide_impl(di, q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, Hkv, N, d,
+                         causal, scale, dtype, stream);
   BwdLaunch a;
   const CUtensorMapDataType dt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;

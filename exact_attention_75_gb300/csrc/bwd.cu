@@ -1130,23 +1130,40 @@ cudaError_t launch_main(const BwdLaunch& a) {
                            dq_configured, a, a.params.BH * a.params.n_qtiles);
 }
 
+// D_i = sum_c dO_ic O_ic for every row of O / dO: every (batch, head) holds
+// N rows, a packed variable-length batch N per head.
 template <int D, bool BF16>
-cudaError_t launch_all(const BwdLaunch& a) {
-  const BwdParams& p = a.params;
-  // rows of O / dO: every (batch, head) holds N, a packed variable-length
-  // batch holds N per head
+cudaError_t launch_pre(const BwdParams& p, int num_sms, cudaStream_t stream) {
   const long rows = (long)(p.cu_seqlens != nullptr ? p.heads : p.BH) * p.N;
   long blocks = (rows + 7) / 8;
-  const long cap = (long)a.num_sms * 16;
+  const long cap = (long)num_sms * 16;
   if (blocks > cap) blocks = cap;
-  bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, a.stream>>>(
+  bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(
       static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.delta, rows);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_all(const BwdLaunch& a) {
+  cudaError_t e = launch_pre<D, BF16>(a.params, a.num_sms, a.stream);
   if (e != cudaSuccess) return e;
   return a.causal ? launch_main<D, true, BF16>(a) : launch_main<D, false, BF16>(a);
 }
 
 }  // namespace
+
+cudaError_t launch_bwd_pre(const BwdParams& p, int d, bool bf16, int num_sms,
+                           cudaStream_t stream) {
+  if (d == 256)
+    return bf16 ? launch_pre<256, true>(p, num_sms, stream) : launch_pre<256, false>(p, num_sms, stream);
+  if (d == 192)
+    return bf16 ? launch_pre<192, true>(p, num_sms, stream) : launch_pre<192, false>(p, num_sms, stream);
+  if (d == 128)
+    return bf16 ? launch_pre<128, true>(p, num_sms, stream) : launch_pre<128, false>(p, num_sms, stream);
+  if (d == 96)
+    return bf16 ? launch_pre<96, true>(p, num_sms, stream) : launch_pre<96, false>(p, num_sms, stream);
+  return bf16 ? launch_pre<64, true>(p, num_sms, stream) : launch_pre<64, false>(p, num_sms, stream);
+}
 
 cudaError_t launch_bwd(const BwdLaunch& a) {
   if (a.d == 64) return a.bf16 ? launch_all<64, true>(a) : launch_all<64, false>(a);

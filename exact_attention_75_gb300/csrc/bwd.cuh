@@ -49,4 +49,23 @@ struct BwdLaunch {
 
 cudaError_t launch_bwd(const BwdLaunch& a);
 
+// The D pass alone (D_i = sum_c dO_ic O_ic into params.delta), any head dim.
+cudaError_t launch_bwd_pre(const BwdParams& p, int d, bool bf16, int num_sms,
+                           cudaStream_t stream);
+
+// Head dims 192 and 256 (bwd_wide.cu): the dK/dV kernel reads Q and dO in
+// tiles of 64 rows, the dQ kernel K and V in tiles of 64 rows, so both sets
+// of tensor maps are needed.  Dense or grouped heads only.
+struct BwdWideLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmDO;          // boxes of 64 columns x 128 rows
+  CUtensorMap tmQ64, tmK64, tmV64, tmDO64;  // boxes of 64 columns x 64 rows
+  BwdParams params;
+  int num_sms;
+  cudaStream_t stream;
+  bool causal, bf16;
+  int d;                                    // 192 or 256
+};
+
+cudaError_t launch_bwd_wide(const BwdWideLaunch& a);
+
 }  // namespace attn

@@ -20,7 +20,10 @@
  *  - Layout: Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d] row-major and
  *    contiguous (d innermost); LSE and the delta vector D are [B, H, N].
  *    All pointers are DEVICE pointers, 16-byte aligned (TMA requirement).
- *  - Shapes: d in {64, 96, 128} (the FP8 entry points: as stated there);
+ *  - Shapes: d in {64, 96, 128}; attn_fwd, attn_fwd_gqa, attn_bwd,
+ *    attn_bwd_gqa and attn_bwd_noalloc also take d in {192, 256} (the key
+ *    split, key cache and variable-length entry points return
+ *    ATTN_ERR_UNSUPPORTED there; the FP8 entry points: as stated there);
  *    N >= 1 (any N: partial tiles are zero-filled on load and masked);
  *    B, H >= 1; B*H*N*d must fit in 2^31 elements.
  *  - Causal masking is top-left aligned: key j is visible to query i iff
@@ -64,8 +67,11 @@ typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype;
  *   o       : [B,H,N,d] same dtype, written (round to nearest even).
  *   lse     : [B,H,N] fp32, written.
  *   causal  : 0 or 1.
+ *   d       : 64, 96, 128, 192 or 256.
  * Cite: FlashAttention-2 review, flowchart "프레임워크 개요" and "Methods";
- * causal block skipping in "핵심 구성요소".
+ * causal block skipping in "핵심 구성요소".  d in {192, 256} computes the
+ * same formulas with wider heads (an extension: the pages' workloads use
+ * d = 64 and 128); those run one 128-row query tile per work unit.
  */
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int N, int d, int causal, float scale, attn_dtype dtype,
@@ -159,10 +165,10 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *   workspace        : >= attn_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte
  *                      aligned, caller-owned; contents on entry are ignored
  *                      and on return are unspecified.
- * d in {64, 96, 128} (ATTN_ERR_UNSUPPORTED otherwise).  dK, dV (per key tile)
- * and dQ (per query tile) are each
- * accumulated in fp32 by one CTA in a fixed order, so the results are the
- * same from run to run.
+ * d in {64, 96, 128, 192, 256} (ATTN_ERR_UNSUPPORTED otherwise).  dK, dV
+ * (per key tile; at d = 256 per key tile and half of the columns) and dQ (per
+ * query tile) are each accumulated in fp32 by one CTA in a fixed order, so
+ * the results are the same from run to run.
  * Cite: FlashAttention-2 review, "Methods" (log-sum-exp kept for the backward
  * pass) and "핵심 구성요소" (backward recomputation with the log-sum-exp).
  */
@@ -237,8 +243,8 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
  * same dQ, dK, dV as attn_bwd, with the same arguments minus the workspace;
  * the scratch (the fp32 delta vector) lives in a fixed device array inside
  * the library.
- *   Limit: B*H*N <= 4194304 query rows and d in {64, 96, 128}; larger problems return
- *   ATTN_ERR_INVALID_ARG, other head dims ATTN_ERR_UNSUPPORTED.
+ *   Limit: B*H*N <= 4194304 query rows and d in {64, 96, 128, 192, 256}; larger
+ *   problems return ATTN_ERR_INVALID_ARG, other head dims ATTN_ERR_UNSUPPORTED.
  *   Memory: the array (16 MB) is part of the library image and is held on
  *   every GPU that loads the library until the process exits.
  *   Sharing: all calls use the same array: calls that overlap on the GPU
