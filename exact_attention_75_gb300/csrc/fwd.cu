@@ -518,6 +518,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nb; ++j) {
         const uint32_t spar = s_it & 1;
         ++s_it;
+        // E4M3: keys [0,64) and [64,128) of the block have their own K and V
+        // scales; they are read before the wait for S, off its critical path.
+        float g0 = 1.f, g1 = 1.f, f0 = 1.f, f1 = 1.f;
+        if constexpr (FP8) {
+          const int b0 = 2 * (w.kb0 + j), b1 = min(b0 + 1, p.n_sblocks - 1);
+          f0 = fq * __ldg(ksc + b0);
+          f1 = fq * __ldg(ksc + b1);
+          g0 = __ldg(vsc + b0) / sv_max;
+          g1 = __ldg(vsc + b1) / sv_max;
+        }
         if (!aborted)
           aborted = !__all_sync(0xffffffffu, mbar_wait(bar(L::kSFull + t), spar, wd, 11));
         if (!aborted) {
@@ -529,18 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
         float s[128];
-        // E4M3: keys [0,64) and [64,128) of the block have their own K and V
-        // scales; the raw scores are scaled inside the exponent argument
-        // (f0 / f1 include the Q scale and scale * log2 e) and the row max is
-        // taken per half on the raw scores (scaling by f > 0 keeps the order).
-        float g0 = 1.f, g1 = 1.f, f0 = 1.f, f1 = 1.f;
-        if constexpr (FP8) {
-          const int b0 = 2 * (w.kb0 + j), b1 = min(b0 + 1, p.n_sblocks - 1);
-          f0 = fq * ksc[b0];
-          f1 = fq * ksc[b1];
-          g0 = vsc[b0] / sv_max;
-          g1 = vsc[b1] / sv_max;
-        }
+        // E4M3: the raw scores are scaled inside the exponent argument (f0 /
+        // f1 include the Q scale and scale * log2 e) and the row max is taken
+        // per half on the raw scores (scaling by f > 0 keeps the order).
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -574,31 +575,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           m_blk = row_max128(s) * sl2;
         }
+        // Raise the reference max where the block's exceeds it by more than
+        // the threshold; O and l of those rows are rescaled by alpha below,
+        // after the exponentials (the scores are dead by then, so O moves
+        // through registers in large pieces with few waits).
+        bool rescale = false;
+        float alpha = 1.f;
         if (j == 0) {
           m = m_blk;
         } else {
           const bool need = m_blk > m + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            // Raise the reference max and rescale this row of O and l.  The
-            // previous P V has completed: its MMA was issued before the S
-            // whose completion we just waited for.
-            const float m_new = need ? m_blk : m;
-            const float alpha = ex2_approx(m - m_new);
-            l *= alpha;
-            m = m_new;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t raw[32];
-              tmem_ld32_sync(o_addr + c * 32, raw);
-              uint32_t lo[16], hi[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                lo[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-                hi[i] = __float_as_uint(__uint_as_float(raw[16 + i]) * alpha);
-              }
-              tmem_st16(o_addr + c * 32, lo);
-              tmem_st16(o_addr + c * 32 + 16, hi);
-            }
+          rescale = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha = ex2_approx(m - m_blk);
+            m = m_blk;
           }
         }
         const float mref = (m == -INFINITY) ? 0.f : m;
@@ -647,7 +637,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float2 rsum = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
-        l += rsum.x + rsum.y;
+        l = l * alpha + (rsum.x + rsum.y);
+        if (rescale) {
+          // O_row *= alpha (1 for rows whose max did not rise).  The previous
+          // P V into O has completed: its MMA was issued before the S whose
+          // completion this block waited for; the next one is issued only
+          // after this block's P is handed over.
+#pragma unroll 1
+          for (int c = 0; c < kPaddedD<D> / 64; ++c) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32(o_addr + c * 64, ra);
+            tmem_ld32(o_addr + c * 64 + 32, rb);
+            tmem_wait_ld();
+            reg_fence32(ra);
+            reg_fence32(rb);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * alpha);
+              rb[i] = __float_as_uint(__uint_as_float(rb[i]) * alpha);
+            }
+            tmem_st32(o_addr + c * 64, ra);
+            tmem_st32(o_addr + c * 64 + 32, rb);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         }

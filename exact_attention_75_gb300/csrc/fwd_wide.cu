@@ -407,35 +407,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 128; ++c) s[c] = (j * 128 + c > lim) ? -INFINITY : s[c];
           }
           const float m_blk = row_max128(s) * sl2;
+          // Raise the reference max where the block's exceeds it by more
+          // than the threshold; O and l of those rows are rescaled by alpha
+          // after the exponentials (the scores are dead by then).
+          bool rescale = false;
+          float alpha = 1.f;
           if (j == 0) {
             m = m_blk;
           } else {
             const bool need = m_blk > m + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-              // P V(j-1) may still be accumulating into O: wait for it.
-              const uint32_t g = pv_it + j - 1;
-              aborted = !mbar_wait(bar(L::kPvDone), g & 1, wd, 13);
-              aborted = __any_sync(0xffffffffu, aborted);
-              if (!aborted) {
-                tc_fence_after();
-                const float m_new = need ? m_blk : m;
-                const float alpha = ex2_approx(m - m_new);
-                l *= alpha;
-                m = m_new;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                  uint32_t raw[32];
-                  tmem_ld32_sync(o_addr + c * 32, raw);
-                  uint32_t lo[16], hi[16];
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) {
-                    lo[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-                    hi[i] = __float_as_uint(__uint_as_float(raw[16 + i]) * alpha);
-                  }
-                  tmem_st16(o_addr + c * 32, lo);
-                  tmem_st16(o_addr + c * 32 + 16, hi);
-                }
-              }
+            rescale = __any_sync(0xffffffffu, need);
+            if (need) {
+              alpha = ex2_approx(m - m_blk);
+              m = m_blk;
             }
           }
           if (!aborted) {
@@ -460,7 +444,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float2 rsum =
                 __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
-            l += rsum.x + rsum.y;
+            l = l * alpha + (rsum.x + rsum.y);
+            if (rescale) {
+              // P V(j-1) may still be accumulating into O (S(j) was issued
+              // before it): wait for its completion, then O_row *= alpha.
+              const uint32_t g = pv_it + j - 1;
+              aborted = __any_sync(0xffffffffu, !mbar_wait(bar(L::kPvDone), g & 1, wd, 13));
+              if (!aborted) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+                  uint32_t ra[32], rb[32];
+                  tmem_ld32(o_addr + c * 64, ra);
+                  tmem_ld32(o_addr + c * 64 + 32, rb);
+                  tmem_wait_ld();
+                  reg_fence32(ra);
+                  reg_fence32(rb);
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    ra[i] = __float_as_uint(__uint_as_float(ra[i]) * alpha);
+                    rb[i] = __float_as_uint(__uint_as_float(rb[i]) * alpha);
+                  }
+                  tmem_st32(o_addr + c * 64, ra);
+                  tmem_st32(o_addr + c * 64 + 32, rb);
+                }
+              }
+            }
             tmem_wait_st();
             tc_fence_before();
           }
