@@ -772,6 +772,56 @@ def cpu_oracle_sample(budget_s: float = 20.0):
     return fl / dt / 1e12, dt, heads, os.cpu_count()
 
 
+# One entry point on one workload, for profiling a single kernel: the step's
+# components on [2,16,8192,128] causal, and the other head dims' forward and
+# backward on [2,16,8192,d] bf16 causal.
+CASES = ("fwd", "bwd", "quant", "fwd_fp8", "fwd_d64", "bwd_d64", "fwd_d96", "bwd_d96",
+         "fwd_d192", "bwd_d192", "fwd_d256", "bwd_d256")
+
+
+def run_case(name, steps, warmup):
+    import exact_attention_75_gb300 as attn
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    if name in COMPONENTS:
+        st = Step(attn, WORKLOAD, dev, list(COMPONENTS))
+        for c in COMPONENTS:  # every input of the component defined
+            st.run(c)
+        fn = lambda: st.run(name)  # noqa: E731
+        w = WORKLOAD
+    elif name in CASES:
+        kind, d = name.split("_d")
+        w = WORKLOAD.with_(d=int(d))
+        g = torch.Generator(device=dev).manual_seed(1234)
+        shape = (w.B, w.H, w.N, w.d)
+        q, k, v, do = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+                       for _ in range(4))
+        o, lse = attn.fwd(q, k, v, causal=w.causal, scale=w.scale)
+        grads = [torch.empty_like(q) for _ in range(3)]
+        if kind == "fwd":
+            fn = lambda: attn.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)  # noqa
+        else:
+            fn = lambda: attn.bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale,  # noqa
+                                  dq=grads[0], dk=grads[1], dv=grads[2])
+    else:
+        raise SystemExit(f"unknown case {name}; one of {', '.join(CASES)}")
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    status = attn.poll_status()
+    if status[0] != 0:
+        raise RuntimeError(f"device status after case {name}: {status}")
+    return {"case": name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "calls": steps, "ms_per_call": e0.elapsed_time(e1) / max(steps, 1)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -779,6 +829,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="run one entry point on its workload (warmup + steps calls, for "
+                         "profiling one kernel): " + ", ".join(CASES))
     ap.add_argument("--sweeps", action="store_true",
                     help="time the forward at every configuration and sweep point of the "
                          "workloads (one GPU) and print them instead of the step line")
@@ -791,6 +844,11 @@ def main():
     rank, world, local_rank = rank_env(args.gpus)
     peaks = load_peaks()
     w = WORKLOAD
+
+    if args.case is not None:
+        if rank == 0:
+            print(json.dumps(run_case(args.case, args.steps, args.warmup)), flush=True)
+        return
 
     if args.sweeps and args.impl == "gb300":
         if rank != 0:

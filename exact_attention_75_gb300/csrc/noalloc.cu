@@ -55,7 +55,7 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
                                         int causal, float scale, attn_dtype dtype,
                                         void* stream) {
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128 && d != 192 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if ((size_t)B * (size_t)H * (size_t)N > kMaxRows) return ATTN_ERR_INVALID_ARG;
   void* scratch = nullptr;
   const attn_status st = scratch_address(&scratch);

@@ -6,7 +6,7 @@ entry point instead of attn_bwd: it keeps its scratch in a fixed device array
 inside the library, so the call allocates nothing.  It runs the same
 deterministic kernels as attn_bwd (only the address of the delta vector
 differs), so this file requires its dQ, dK, dV to be bitwise equal to
-attn_bwd's, through the C ABI, on two calls in a row for each of four
+attn_bwd's, through the C ABI, on two calls in a row for each of five
 different problems (a stale or misplaced scratch would change the bits),
 checks the first problem against the fp64 oracle at the backward tolerance
 (5e-2 * max |reference|), and checks that oversized problems are rejected.
@@ -49,11 +49,12 @@ def test_noalloc_backward_matches_attn_bwd_twice(attn_lib):
     import oracle
     fn = _noalloc_fn(attn_lib)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    # four different problems through the shared scratch array, each twice
+    # five different problems through the shared scratch array, each twice
     for n, w in enumerate((wl.Workload("na1", "bwd", 1, 4, 1000, 128, "bf16", True, seed=31),
                            wl.Workload("na2", "bwd", 2, 3, 4096, 128, "bf16", False, seed=32),
                            wl.Workload("na3", "bwd", 1, 2, 700, 64, "fp16", True, seed=33),
-                           wl.Workload("na4", "bwd", 2, 1, 390, 96, "bf16", True, seed=34))):
+                           wl.Workload("na4", "bwd", 2, 1, 390, 96, "bf16", True, seed=34),
+                           wl.Workload("na5", "bwd", 1, 2, 333, 256, "bf16", True, seed=35))):
         inp = wl.make_inputs(w)
         q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
         o, lse = attn_lib.fwd(q, k, v, causal=w.causal, scale=w.scale)
