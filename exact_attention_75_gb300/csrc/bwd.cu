@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
-      constexpr uint32_t kIdKV = idesc_f16(128, kPaddedD<D>, BF16, false, true);  // dV, dK
+      constexpr uint32_t kIdKV = idesc_f16(128, D, BF16, false, true);  // dV, dK
       uint32_t st_it = 0;
       bool aborted = false;
       // K and V as K-major A operands of S^T / dP^T.
@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nothing), so every rendezvous pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);  // S, dP
-      constexpr uint32_t kIdQ = idesc_f16(128, kPaddedD<D>, BF16, false, true);  // dQ
+      constexpr uint32_t kIdQ = idesc_f16(128, D, BF16, false, true);  // dQ
       uint32_t k_it = 0, v_it = 0, step_it = 0;
       bool aborted = false;
       const uint64_t qd = kmajor_base(sbase + L::kQ), dod = kmajor_base(sbase + L::kDO);

@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         FP8 ? idesc_e4m3(128, 128, false, false) : idesc_f16(128, 128, BF16, false, false);
     constexpr uint32_t kIdO =
         FP8 ? idesc_e4m3(128, D, false, false)
-            : idesc_f16(128, kPaddedD<D>, BF16, false, true);
+            : idesc_f16(128, D, BF16, false, true);
     uint32_t kv_it = 0;
     bool aborted = false;
     bool issued = false;

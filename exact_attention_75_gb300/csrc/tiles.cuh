@@ -4,8 +4,9 @@
 // column halves, each [128 rows][64 values] = 16 KB, 1024-byte aligned.  A
 // head dim that is not a multiple of 64 (d = 96) occupies the columns of the
 // next multiple: TMA fills the columns past d with zeros, so products that
-// contract over d stop at d, and products with d outputs per row run over the
-// padded width and produce zeros there.
+// contract over d stop at d, and products with d outputs per row are issued
+// with N = d (an MN-major operand of 96 columns reads one and a half 128-byte
+// swizzle atoms from an atom-aligned base).
 #pragma once
 
 #include <cstdint>

@@ -56,15 +56,15 @@ def test_gqa_backward_small(attn_lib, causal, dtype, d, B, Hq, Hkv, N):
 
 def test_gqa_full_size_sampled_heads(attn_lib):
     """[1,16,4096,128] bf16 causal with 4 key/value heads: forward on sampled
-    rows of two query heads, backward of the first key/value group (its 4
-    query heads) against the oracle."""
+    rows of four query heads (the first and the last included), backward of
+    the first key/value group (its 4 query heads) against the oracle."""
     w, q, k, v, do = _make(1, 16, 4, 4096, 128, "bf16", seed=99)
     qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
     o, lse = attn_lib.fwd(qc, kc, vc, causal=True)
     dq, dk, dv = attn_lib.bwd(qc, kc, vc, o, doc, lse, causal=True)
     assert attn_lib.poll_status() == (0, 0)
     rows = np.arange(0, w.N, 157)
-    for h in (0, 13):
+    for h in (0, 6, 9, 15):
         g = oracle.kv_head_of(h, 16, 4)
         O_ref, L_ref = oracle.attention_rows(to64(q[0, h]), to64(k[0, g]), to64(v[0, g]), rows,
                                              True, w.scale)
