@@ -77,6 +77,33 @@ def test_noalloc_backward_matches_attn_bwd_twice(attn_lib):
                 assert np.max(np.abs(to64(g) - r)) <= REL_TOL * np.max(np.abs(r))
 
 
+def test_noalloc_and_bwd_on_two_devices_in_turn(attn_lib):
+    """The shared-memory opt-in of the kernels and the scratch array's
+    address are per device: calls alternating between two GPUs in one
+    process must each run on their own device with the same results as on
+    the first.  Skipped on machines with a single GPU."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two GPUs")
+    fn = _noalloc_fn(attn_lib)
+    w = wl.Workload("na2dev", "bwd", 1, 2, 700, 128, "bf16", True, seed=41)
+    inp = wl.make_inputs(w)
+    results = []
+    for dev in (0, 1, 0, 1):
+        with torch.cuda.device(dev):
+            q, k, v, do = (inp[n].to(f"cuda:{dev}") for n in ("q", "k", "v", "do"))
+            o, lse = attn_lib.fwd(q, k, v, causal=True, scale=w.scale)
+            ref = attn_lib.bwd(q, k, v, o, do, lse, causal=True, scale=w.scale)
+            got = [torch.empty_like(q) for _ in range(3)]
+            stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+            assert _call(fn, q, k, v, o, do, lse, *got, w, stream) == 0
+            assert attn_lib.poll_status()[0] == 0
+            for g, r in zip(got, ref):
+                assert torch.equal(g, r)
+            results.append([t.cpu() for t in got])
+    for a, b in zip(results[0], results[1]):
+        assert torch.equal(a, b)
+
+
 def test_noalloc_rejects_oversized_problems(attn_lib):
     fn = _noalloc_fn(attn_lib)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
