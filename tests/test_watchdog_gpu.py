@@ -88,3 +88,37 @@ def test_backward_winds_down_when_waits_run_out(attn_lib):
                                      w.scale)
     for g, r in zip((dq, dk, dv), refs):
         assert np.max(np.abs(to64(g) - r)) <= 5e-2 * np.max(np.abs(r))
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_kernels_wind_down_when_waits_run_out(attn_lib, d):
+    """The same for the wide head dims' forward and backward kernels (one
+    query tile per forward unit; the 64-row backward rings), on enough work
+    units that every CTA runs more than one (a producer then waits a whole
+    unit for its next one, which outlasts any 1 us limit): a launch whose
+    waits run out reports ATTN_ERR_TIMEOUT and the next launches at the
+    normal limit match the oracle (two whole heads)."""
+    import numpy as np
+    import oracle
+    from helpers import to64
+    w = wl.Workload("tw", "bwd", 1, 8, 4096, d, "bf16", True, seed=d + 3)
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    attn_lib.poll_status()
+    _expect_timeout(attn_lib, lambda: attn_lib.fwd(q, k, v, causal=True))
+    o, lse = attn_lib.fwd(q, k, v, causal=True)
+    assert attn_lib.poll_status() == (0, 0)
+    _expect_timeout(attn_lib, lambda: attn_lib.bwd(q, k, v, o, do, lse, causal=True))
+    dq, dk, dv = attn_lib.bwd(q, k, v, o, do, lse, causal=True)
+    assert attn_lib.poll_status() == (0, 0)
+    heads = [(0, 0), (0, 7)]
+    refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), True,
+                                     w.scale, heads=heads)
+    for (b, h) in heads:
+        O_ref, L_ref = oracle.attention_rows(to64(inp["q"][b, h]), to64(inp["k"][b, h]),
+                                             to64(inp["v"][b, h]), np.arange(w.N), True,
+                                             w.scale)
+        assert np.max(np.abs(to64(o[b, h]) - O_ref)) <= 2e-2
+        assert np.max(np.abs(to64(lse[b, h]) - L_ref)) <= 5e-3
+        for g, r in zip((dq, dk, dv), refs):
+            assert np.max(np.abs(to64(g[b, h]) - r[b, h])) <= 5e-2 * np.max(np.abs(r[b, h]))
