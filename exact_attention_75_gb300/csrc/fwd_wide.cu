@@ -253,7 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
     bool issued = false;
     const uint64_t qdesc = kmajor_base(sbase + L::kQOff);
-    // S into buffer sb = Q K^T; K's chunks start at ring position it0.
+    // S into buffer sb = Q K^T; K's chunks start at ring position it0.  Each
+    // chunk's slot is released as soon as its own MMAs complete (a commit
+    // right after them), so the producer can refill it while the rest of
+    // the product runs.
     auto issue_s = [&](uint32_t sb, uint32_t it0) {
       const uint32_t dcol = tbase + 128 * sb;
 #pragma unroll
@@ -263,9 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma_f16_ss(dcol, desc_plus(qdesc, kmajor16_off(4 * c + kk)),
                      desc_plus(kd, kmajor16_off(kk)), kIdS, (c | kk) ? 1u : 0u);
+        mma_commit(bar(L::kKvEmpty + (it0 + c) % L::kRing));
       }
     };
-    // O[:, 64c, 64c+64) += P V_c for each chunk c of V (at ring position it0).
+    // O[:, 64c, 64c+64) += P V_c for each chunk c of V (at ring position
+    // it0), each chunk's slot released after its MMAs.
     auto issue_pv = [&](uint32_t sb, uint32_t it0, uint32_t acc0) {
       const uint32_t pcol = tbase + 128 * sb;
 #pragma unroll
@@ -275,11 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA
           mma_f16_ts(tbase + 256 + 64 * c, pcol + kk * 8, desc_plus(vd, mnmajor16_off(kk)), kIdO,
                      kk > 0 ? 1u : acc0);
+        mma_commit(bar(L::kKvEmpty + (it0 + c) % L::kRing));
       }
-    };
-    auto release = [&](uint32_t it0) {
-#pragma unroll
-      for (int c = 0; c < CH; ++c) mma_commit(bar(L::kKvEmpty + (it0 + c) % L::kRing));
     };
     for (int k = 0;; ++k) {
       const int u = snake_unit(k, cta, G);
@@ -297,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           issue_s(s0 & 1, k0pos);
           mma_commit(bar(L::kSFull + (s0 & 1)));
-          release(k0pos);
           if (nb == 1) mma_commit(bar(L::kQEmpty));
         }
         issued = true;
@@ -312,7 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             issue_s((s0 + 1) & 1, k1pos);
             mma_commit(bar(L::kSFull + ((s0 + 1) & 1)));
-            release(k1pos);
             if (nb == 2) mma_commit(bar(L::kQEmpty));
           }
           __syncwarp();
@@ -337,14 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sb = (s0 + j) & 1;
             issue_pv(sb, vpos, j > 0 ? 1u : 0u);
             mma_commit(bar(L::kPvDone));
-            release(vpos);
             if (j == nb - 1) mma_commit(bar(L::kOFull));
             if (next) {
               // S(j+2) reuses the buffer of block j (its P was read by the
               // P V just issued; MMAs of this thread execute in order).
               issue_s(sb, k2pos);
               mma_commit(bar(L::kSFull + sb));
-              release(k2pos);
               if (j + 2 == nb - 1) mma_commit(bar(L::kQEmpty));
             }
           }
