@@ -87,8 +87,11 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
 // Per step s the tensor core runs S^T(s) | dK(s-1) | dP^T(s) | dV(s), so the
 // warpgroups' P^T(s) overlaps dK(s-1) and dP^T(s), and their dS^T(s)
 // overlaps dV(s) and S^T(s+1).  Q_i is then read until the next step (by
-// dK), so Q has a ring of 3 slots; dO_i and the -LSE / -D vectors of its
-// queries have one of 2 slots.
+// dK), so Q has a ring of 3 slots.  dO_i is last read by dV(s) and has a
+// ring of 2 slots, each freed as soon as dV(s) completes; the -LSE / -D
+// vectors of its queries are last read by the warpgroups' dS^T(s) phase and
+// have a ring of their own (2 slots), so the next dO load need not wait for
+// that phase and for dK(s).
 template <int D>
 struct DkvLayout {
   static constexpr int kTile = kTileBytes<D>;
@@ -97,11 +100,12 @@ struct DkvLayout {
   static constexpr int kQSlots = 3, kDoSlots = 2;
   static constexpr int kQ0 = 2 * kTile;
   static constexpr int kDo0 = kQ0 + kQSlots * kTile;
-  static constexpr int kVec = kDo0 + kDoSlots * kTile;  // per dO slot: -LSE2[128], -D[128]
+  static constexpr int kVec = kDo0 + kDoSlots * kTile;  // per vector slot: -LSE2[128], -D[128]
   static constexpr int kBar = kVec + kDoSlots * 1024;
   enum {
     kKvFull, kKvEmpty, kQFull, kQEmpty = kQFull + kQSlots, kDoFull = kQEmpty + kQSlots,
-    kDoEmpty = kDoFull + kDoSlots, kSFull = kDoEmpty + kDoSlots, kDpFull, kPReady, kDsReady,
+    kDoEmpty = kDoFull + kDoSlots, kVecEmpty = kDoEmpty + kDoSlots,
+    kSFull = kVecEmpty + kDoSlots, kDpFull, kPReady, kDsReady,
     kDkvFull, kDkvFree, kDrain, kNumBars
   };
   static constexpr int kMisc = kBar + kNumBars * 8;
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::kDoSlots; ++s) {
       mbar_init(bar(L::kDoFull + s), 2);  // TMA bytes + the -LSE/-D writer
       mbar_init(bar(L::kDoEmpty + s), 1);
+      mbar_init(bar(L::kVecEmpty + s), 8);  // one arrival per compute warp
     }
     mbar_init(bar(L::kSFull), 1);
     mbar_init(bar(L::kDpFull), 1);
@@ -275,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_tile<D>(sbase + L::kDo0 + ds * kTile, &tmDO, bar(L::kDoFull + ds),
                       w.row0 + i * 128, zq);
             ++do_issued;
+            ok = mbar_wait(bar(L::kVecEmpty + ds), ((st_it / L::kDoSlots) & 1) ^ 1, wd, 37);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -327,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool aborted = false;
       // K and V as K-major A operands of S^T / dP^T.
       const uint64_t kd_k = kmajor_base(sbase + L::kK), vd_k = kmajor_base(sbase + L::kV);
-      // dK(s) += dS^T(s) Q_i(s) with Q from its ring slot; then the slots of
-      // step s are free (its dS^T phase, the last reader of its -D, is done).
+      // dK(s) += dS^T(s) Q_i(s) with Q from its ring slot; then Q's slot is
+      // free.
       auto issue_dk = [&](uint32_t step, uint32_t acc0) {
         const uint32_t qs = step % L::kQSlots;
         const uint64_t qd_mn = mnmajor_base(sbase + L::kQ0 + qs * kTile);
@@ -337,7 +343,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16_ts(tbase + kColDK, tbase + kColDP + half_packed_col(kk),
                      desc_plus(qd_mn, mnmajor16_off(kk)), kIdKV, kk > 0 ? 1u : acc0);
         mma_commit(bar(L::kQEmpty + qs));
-        mma_commit(bar(L::kDoEmpty + step % L::kDoSlots));
       };
       for (int k = 0;; ++k) {
         const int u = snake_unit(k, cta, G);
@@ -390,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 8; ++kk)
               mma_f16_ts(tbase + kColDV, tbase + kColS + half_packed_col(kk),
                          desc_plus(dod_mn, mnmajor16_off(kk)), kIdKV, kk > 0 || s > 0 ? 1u : 0u);
+            mma_commit(bar(L::kDoEmpty + ds));  // dV(s) was the last reader of dO_i
           }
           ++st_it;
         }
@@ -471,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ds = st_it % L::kDoSlots;
         const uint32_t par = st_it & 1;
         ok = mbar_wait(bar(L::kSFull), par, wd, 33);
-        // the -LSE / -D vectors travel with dO_i
+        // dO_i's full barrier also waits for the -LSE / -D vectors' writer
         ok = ok && mbar_wait(bar(L::kDoFull + ds), (st_it / L::kDoSlots) & 1, wd, 34);
         // Exit decisions are uniform over the warpgroup (its warps meet at
         // named barriers).
@@ -561,6 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::kDsReady));
+        // this warp has read its -LSE / -D for the step
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kVecEmpty + ds));
         ++st_it;
       }
       if (!ok) break;
