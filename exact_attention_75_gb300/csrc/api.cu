@@ -137,6 +137,23 @@ cudaError_t launch_varlen_check(const int* cu, int n_seq, int total, int max_seq
   return cudaGetLastError();
 }
 
+// Bytes of the backward's delta vector (fp32 per query row), rounded up to
+// 256; the work counters follow it in the workspace.
+size_t bwd_delta_bytes(int B, int H, int N) {
+  return ((size_t)B * H * N * 4 + 255) & ~(size_t)255;
+}
+
+// Heads per block of the backward's causal unit order: as many as keep the
+// tiles that one block's units stream (per_head bytes each) within 32 MiB of
+// L2, at least 4 (so that enough units of similar length are in flight for
+// the CTAs to finish together) and at most all of them.
+int bwd_head_block(double per_head, int total) {
+  int hb = (int)(33554432.0 / per_head);
+  if (hb < 4) hb = 4;
+  if (hb > total) hb = total;
+  return hb < 1 ? 1 : hb;
+}
+
 bool head_dim_ok(int d) { return d == 64 || d == 96 || d == 128 || d == 192 || d == 256; }
 
 bool shape_ok(int B, int H, int N, int d) {
@@ -348,8 +365,8 @@ attn_status attn_merge(const void* o_part, const float* lse_part, int n_split, v
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (!shape_ok(B, H, N, d)) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return (rows * 4 + 255) & ~(size_t)255;  // D = rowsum(dO o O), fp32
+  // D = rowsum(dO o O), fp32, then 256 bytes for the main kernels' work counters
+  return bwd_delta_bytes(B, H, N) + 256;
 }
 
 }  // extern "C"
@@ -478,6 +495,14 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  p.sched = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                   bwd_delta_bytes(varlen ? 1 : B, H, N));
+  // A head's two streamed tensors (rows x padded d, 16-bit): dK/dV units
+  // stream Q and dO of a key/value head's whole group, dQ units K and V,
+  // which the group's query heads share.
+  const double head_bytes = (double)(varlen ? max_seqlen : N) * ((d + 63) / 64 * 64) * 4.0;
+  p.head_block = bwd_head_block(head_bytes * p.group, p.BHkv);
+  p.head_block_q = bwd_head_block(head_bytes / p.group, p.BH);
   a.num_sms = di->num_sms;
   a.stream = static_cast<cudaStream_t>(stream);
   a.causal = causal != 0;

@@ -7,7 +7,8 @@
 // Attention v3" is staged; here the stages are
 //   1. bwd_pre_kernel  D_i = sum_c dO_ic O_ic (warp-shuffle row reduction);
 //   2. bwd_dkv_kernel  one CTA per 128-key K/V tile (persistent, longest
-//                      first): for every 128-query tile i it recomputes
+//                      first within a block of heads): for every 128-query
+//                      tile i it recomputes
 //                      S^T = K Q_i^T and P^T = exp2(S^T c - LSE_i log2 e),
 //                      dP^T = V dO_i^T, dS^T = P^T o (dP^T - D_i), and
 //                      accumulates dV += P^T dO_i, dK += dS^T Q_i in tensor
@@ -35,6 +36,13 @@
 //   warp 10          relay: waits on the pipeline's mbarriers and
 //                    meets the issuer at a named barrier, so that the issuer
 //                    never touches shared memory between its commits
+// Units (a K/V tile, or a query tile) are handed out at run time: the
+// producer takes the next one from a counter in the workspace with an atomic
+// add and publishes it through a small ring in shared memory (kUnitSlots
+// entries), which the issuer, the relay and the compute warps read; an entry
+// of -1 ends the CTA's work.  A CTA that finishes early takes more units, and
+// with the causal order blocked by heads the units in flight at any time
+// stream the tiles of a few heads only, which then stay in L2.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -56,6 +64,10 @@ constexpr int kWarpRelay = 10;
 constexpr uint32_t kBarRelay = 3;  // named barrier: relay warp + issuer warp (64 threads)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStatusLayout = 5;  // shared memory not 1024-byte aligned
+// Unit ring: entries published by the producer; each is released by the
+// issuer, the relay and the 8 compute warps (one arrival each).
+constexpr int kUnitSlots = 4;
+constexpr int kUnitReaders = 10;
 // Bytes of a 128-row tile of 16-bit values with D columns (padded to a
 // multiple of 64).
 template <int D>
@@ -70,6 +82,46 @@ __device__ __forceinline__ uint32_t half_packed_col(int kk) {
 
 __device__ __forceinline__ uint32_t pack16x2(bool bf16, float lo, float hi) {
   return bf16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+
+// Producer side of the unit ring (one thread): once entry un's slot has been
+// released, takes the next unit from the counter and publishes it (-1 once
+// the counter has passed num_units).  Returns the unit, or -1 with ok false
+// when the wait ran out.
+__device__ __forceinline__ int publish_unit(volatile int* ring, uint32_t full0, uint32_t empty0,
+                                            uint32_t un, int* counter, int num_units,
+                                            const Watchdog& wd, bool& ok, int site) {
+  const uint32_t us = un % kUnitSlots;
+  ok = mbar_wait(empty0 + 8u * us, ((un / kUnitSlots) & 1) ^ 1, wd, site);
+  if (!ok) return -1;
+  int u = atomicAdd(counter, 1);
+  if (u >= num_units) u = -1;
+  ring[us] = u;
+  mbar_arrive(full0 + 8u * us);
+  return u;
+}
+
+// Reader side (every lane of a warp): waits for entry un, reads it and
+// releases it with one arrival for the warp.  Returns -1 with ok false when
+// the wait ran out.
+__device__ __forceinline__ int take_unit(volatile int* ring, uint32_t full0, uint32_t empty0,
+                                         uint32_t un, const Watchdog& wd, bool& ok, int site) {
+  const uint32_t us = un % kUnitSlots;
+  ok = mbar_wait(full0 + 8u * us, (un / kUnitSlots) & 1, wd, site);
+  const int u = ok ? ring[us] : -1;
+  __syncwarp();
+  if (ok && (threadIdx.x & 31) == 0) mbar_arrive(empty0 + 8u * us);
+  return u;
+}
+
+// The same for the relay / issuer pair: the relay has waited for entry un and
+// met the issuer at their named barrier, so both read it and release it.
+__device__ __forceinline__ int read_unit(volatile int* ring, uint32_t empty0, uint32_t un) {
+  const uint32_t us = un % kUnitSlots;
+  const int u = ring[us];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty0 + 8u * us);
+  return u;
 }
 
 // Loads a 128 x D 16-bit tile (boxes of 64 columns; columns past D are
@@ -106,10 +158,11 @@ struct DkvLayout {
     kKvFull, kKvEmpty, kQFull, kQEmpty = kQFull + kQSlots, kDoFull = kQEmpty + kQSlots,
     kDoEmpty = kDoFull + kDoSlots, kVecEmpty = kDoEmpty + kDoSlots,
     kSFull = kVecEmpty + kDoSlots, kDpFull, kPReady, kDsReady,
-    kDkvFull, kDkvFree, kDrain, kNumBars
+    kDkvFull, kDkvFree, kDrain, kUnitFull, kUnitEmpty = kUnitFull + kUnitSlots,
+    kNumBars = kUnitEmpty + kUnitSlots
   };
-  static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM address, abort flag, unit ring
+  static constexpr int kBytes = kMisc + 16 + 4 * kUnitSlots;
   static_assert(kBytes <= 232448, "shared memory budget (227 KB) exceeded");
 };
 
@@ -153,9 +206,15 @@ template <bool CAUSAL>
 __device__ __forceinline__ DkvUnit decode_dkv_unit(int u, const BwdParams& p) {
   DkvUnit w;
   if (CAUSAL || p.cu_seqlens != nullptr) {
-    // K/V tile j sees query tiles j..n-1: ascending j is longest first.
-    w.j = u / p.BHkv;
-    w.bhkv = u - w.j * p.BHkv;
+    // K/V tile j sees query tiles j..n-1: ascending j is longest first,
+    // within blocks of head_block heads (the last block may be smaller).
+    const int per_blk = p.head_block * p.n_kblocks;
+    const int blk = u / per_blk;
+    const int r = u - blk * per_blk;
+    const int h0 = blk * p.head_block;
+    const int hb = min(p.head_block, p.BHkv - h0);
+    w.j = r / hb;
+    w.bhkv = h0 + (r - w.j * hb);
   } else {
     w.bhkv = u / p.n_kblocks;
     w.j = u - w.bhkv * p.n_kblocks;
@@ -197,12 +256,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   Watchdog wd{p.status, abort_flag, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(bar(L::kUnitFull + s), 1);
+      mbar_init(bar(L::kUnitEmpty + s), kUnitReaders);
+    }
     mbar_init(bar(L::kKvFull), 1);
     mbar_init(bar(L::kKvEmpty), 1);
     for (int s = 0; s < L::kQSlots; ++s) {
@@ -231,8 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
-  const int G = gridDim.x;
-  const int cta = blockIdx.x;
   const int num_units = p.BHkv * p.n_kblocks;
 
   if (warp == kWarpProducer) {
@@ -243,12 +305,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
     }
-    uint32_t kv_it = 0, st_it = 0;
+    uint32_t kv_it = 0, st_it = 0, un = 0;
     uint32_t q_issued = 0, do_issued = 0;  // copies issued (lane 0), for the drain
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    while (ok) {
+      int u = -1;
+      if (lane == 0)
+        u = publish_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un, p.sched, num_units,
+                         wd, ok, 38);
+      ++un;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!ok || u < 0) break;
       const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
       if (w.nsteps == 0) continue;
       if (lane == 0) {
@@ -324,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Per step s: S^T(s) | dK(s-1) | dP^T(s) | dV(s); after the unit's last
     // step its dK.  Each group is issued after a rendezvous with the relay
     // warp, which has seen its inputs complete; after an abort both warps
-    // still walk the whole schedule (issuing nothing), so every rendezvous
-    // pairs up.
+    // walk the rest of the unit (issuing nothing) and leave together at the
+    // next unit's rendezvous, so every rendezvous pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_f16(128, D, BF16, false, true);  // dV, dK
@@ -344,9 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                      desc_plus(qd_mn, mnmajor16_off(kk)), kIdKV, kk > 0 ? 1u : acc0);
         mma_commit(bar(L::kQEmpty + qs));
       };
-      for (int k = 0;; ++k) {
-        const int u = snake_unit(k, cta, G);
-        if (u >= num_units) break;
+      for (uint32_t un = 0;; ++un) {
+        // the relay has seen the next unit published (after an abort both
+        // warps leave here, having met at every rendezvous so far)
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if (aborted) break;
+        const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+        if (u < 0) break;
         const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
         for (int s = 0; s < w.nsteps; ++s) {
@@ -428,9 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint32_t b, uint32_t par, int site) {
       if (!aborted) aborted = !__all_sync(0xffffffffu, mbar_wait(b, par, wd, site));
     };
-    for (int k = 0;; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    for (uint32_t un = 0;; ++un) {
+      wait_all(bar(L::kUnitFull + un % kUnitSlots), (un / kUnitSlots) & 1, 39);
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      if (aborted) break;
+      const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+      if (u < 0) break;
       const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
       if (w.nsteps == 0) continue;
       wait_all(bar(L::kKvFull), kv_it & 1, 25);
@@ -463,11 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = tbase + lane_base + kColS + 64 * h;
     const uint32_t dp_addr = tbase + lane_base + kColDP + 64 * h;
     const float sl2 = p.scale_log2;
-    uint32_t st_it = 0, unit_it = 0;
+    uint32_t st_it = 0, unit_it = 0, un = 0;
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    while (ok) {
+      const int u = take_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un++, wd, ok, 40);
+      ok = named_bar_and(1 + h, 128, ok);
+      if (!ok || u < 0) break;
       const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
       if (w.nsteps == 0) continue;
       for (int s = 0; s < w.nsteps; ++s) {
@@ -631,10 +707,11 @@ struct DqLayout {
   enum {
     kQFull, kQEmpty, kKFull, kKEmpty = kKFull + kKSlots, kVFull = kKEmpty + kKSlots,
     kVEmpty = kVFull + kVSlots, kSFull = kVEmpty + kVSlots, kSRead = kSFull + 2, kDpFull,
-    kDsReady, kDqFull, kDqFree, kDrain, kNumBars
+    kDsReady, kDqFull, kDqFree, kDrain, kUnitFull, kUnitEmpty = kUnitFull + kUnitSlots,
+    kNumBars = kUnitEmpty + kUnitSlots
   };
-  static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM address, abort flag, unit ring
+  static constexpr int kBytes = kMisc + 16 + 4 * kUnitSlots;
   static_assert(kBytes <= 232448, "shared memory budget (227 KB) exceeded");
 };
 
@@ -655,9 +732,15 @@ template <bool CAUSAL>
 __device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
   DqUnit w;
   if (CAUSAL || p.cu_seqlens != nullptr) {
-    // Query tile i sees key tiles 0..i: descending i is longest first.
-    const int r = u / p.BH;
-    w.bh = u - r * p.BH;
+    // Query tile i sees key tiles 0..i: descending i is longest first,
+    // within blocks of head_block_q heads (the last block may be smaller).
+    const int per_blk = p.head_block_q * p.n_qtiles;
+    const int blk = u / per_blk;
+    const int r0 = u - blk * per_blk;
+    const int h0 = blk * p.head_block_q;
+    const int hb = min(p.head_block_q, p.BH - h0);
+    const int r = r0 / hb;
+    w.bh = h0 + (r0 - r * hb);
     w.i = p.n_qtiles - 1 - r;
   } else {
     w.bh = u / p.n_qtiles;
@@ -698,12 +781,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   Watchdog wd{p.status, abort_flag, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(bar(L::kUnitFull + s), 1);
+      mbar_init(bar(L::kUnitEmpty + s), kUnitReaders);
+    }
     mbar_init(bar(L::kQFull), 1);
     mbar_init(bar(L::kQEmpty), 1);
     for (int s = 0; s < L::kKSlots; ++s) {
@@ -731,8 +819,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
-  const int G = gridDim.x;
-  const int cta = blockIdx.x;
   const int num_units = p.BH * p.n_qtiles;
 
   if (warp == kWarpProducer) {
@@ -742,11 +828,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      uint32_t k_it = 0, v_it = 0, unit_it = 0;
+      uint32_t k_it = 0, v_it = 0, unit_it = 0, un = 0;
       bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int u = snake_unit(k, cta, G);
-        if (u >= num_units) break;
+      while (ok) {
+        const int u = publish_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un++,
+                                   p.sched + 1, num_units, wd, ok, 38);
+        if (u < 0) break;
         const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
         ok = mbar_wait(bar(L::kQEmpty), (unit_it & 1) ^ 1, wd, 41);
@@ -791,8 +878,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warpgroups have read S_j.  The warpgroups compute P_j while dQ and dP_j
     // run, and dS_j while S_{j+1} runs.  Each group is issued after a
     // rendezvous with the relay warp, which has seen its inputs complete.
-    // After an abort both warps still walk the whole schedule (issuing
-    // nothing), so every rendezvous pairs up.
+    // After an abort both warps walk the rest of the unit (issuing nothing)
+    // and leave together at the next unit's rendezvous, so every rendezvous
+    // pairs up.
     {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);  // S, dP
       constexpr uint32_t kIdQ = idesc_f16(128, D, BF16, false, true);  // dQ
@@ -807,9 +895,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16_ts(tbase + kColDQ, tbase + kColS0 + 128 * sb + half_packed_col(kk),
                      desc_plus(kd_mn, mnmajor16_off(kk)), kIdQ, kk > 0 ? 1u : acc0);
       };
-      for (int k = 0;; ++k) {
-        const int u = snake_unit(k, cta, G);
-        if (u >= num_units) break;
+      for (uint32_t un = 0;; ++un) {
+        // the relay has seen the next unit published (after an abort both
+        // warps leave here, having met at every rendezvous so far)
+        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if (aborted) break;
+        const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+        if (u < 0) break;
         const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
         uint32_t prev_kaddr = 0, prev_ks = 0, prev_sb = 0;
@@ -899,9 +991,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint32_t b, uint32_t par, int site) {
       if (!aborted) aborted = !__all_sync(0xffffffffu, mbar_wait(b, par, wd, site));
     };
-    for (int k = 0;; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    for (uint32_t un = 0;; ++un) {
+      wait_all(bar(L::kUnitFull + un % kUnitSlots), (un / kUnitSlots) & 1, 39);
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      if (aborted) break;
+      const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+      if (u < 0) break;
       const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
       if (w.nsteps == 0) continue;
       for (int j = 0; j < w.nsteps; ++j) {
@@ -932,11 +1027,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t dq_addr = tbase + lane_base + kColDQ;
     const float sl2 = p.scale_log2;
-    uint32_t unit_it = 0, step_it = 0;
+    uint32_t unit_it = 0, step_it = 0, un = 0;
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    while (ok) {
+      const int u = take_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un++, wd, ok, 40);
+      ok = named_bar_and(1 + h, 128, ok);
+      if (!ok || u < 0) break;
       const DqUnit w = decode_dq_unit<CAUSAL>(u, p);
       if (w.nsteps == 0) continue;
       const int row = w.i * 128 + r;
@@ -1069,8 +1165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                      const uint16_t* __restrict__ dout,
-                                                     float* __restrict__ delta, long rows) {
+                                                     float* __restrict__ delta, long rows,
+                                                     int* __restrict__ sched) {
   constexpr int W = (D + 63) / 64;  // 32-bit words (two values each) per lane, at most
+  // the main kernels' work counters start at 0 (they run after this kernel
+  // on the same stream)
+  if (sched != nullptr && blockIdx.x == 0 && threadIdx.x < 2) sched[threadIdx.x] = 0;
   const long warp0 = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -1148,7 +1248,8 @@ cudaError_t launch_pre(const BwdParams& p, int num_sms, cudaStream_t stream) {
   const long cap = (long)num_sms * 16;
   if (blocks > cap) blocks = cap;
   bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(
-      static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.delta, rows);
+      static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.delta, rows,
+      p.sched);
   return cudaGetLastError();
 }
 

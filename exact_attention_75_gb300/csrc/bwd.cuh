@@ -36,6 +36,13 @@ struct BwdParams {
   float scale;
   float scale_log2;      // scale * log2(e)
   unsigned long long wait_limit_ns;
+  // Work counters of the dK/dV ([0]) and dQ ([1]) kernels in the workspace,
+  // zeroed by the D pass: each CTA takes its next unit with an atomic add.
+  int* sched = nullptr;
+  // Causal and variable-length orders hand out the units of head_block
+  // key/value heads (dK/dV) or head_block_q query heads (dQ) before those of
+  // the next heads, so the tiles the CTAs stream stay in L2.
+  int head_block = 1, head_block_q = 1;
 };
 
 struct BwdLaunch {

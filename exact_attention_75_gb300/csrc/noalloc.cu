@@ -22,8 +22,9 @@
 namespace {
 
 constexpr size_t kMaxRows = 4194304;  // B * H * N of one call
-// The workspace attn_bwd expects: delta, fp32 per row (a multiple of 256 bytes).
-constexpr size_t kScratchBytes = kMaxRows * 4;
+// The workspace attn_bwd expects: delta, fp32 per row (a multiple of 256
+// bytes), then 256 bytes of work counters.
+constexpr size_t kScratchBytes = kMaxRows * 4 + 256;
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
@@ -60,9 +61,10 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
   void* scratch = nullptr;
   const attn_status st = scratch_address(&scratch);
   if (st != ATTN_OK) return st;
-  // The array holds only the delta vector D.  attn_bwd's D pass writes
-  // delta[row] for every row < B*H*N on this stream before either main
-  // kernel reads it, so leftovers of an earlier call are never read.
+  // The array holds the delta vector D and the work counters.  attn_bwd's D
+  // pass writes delta[row] for every row < B*H*N and zeroes the counters on
+  // this stream before either main kernel reads them, so leftovers of an
+  // earlier call are never read.
   return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, kScratchBytes, B, H, N, d, causal,
                   scale, dtype, stream);
 }

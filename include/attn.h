@@ -150,8 +150,9 @@ attn_status attn_merge(const void* o_part, const float* lse_part, int n_split, v
 
 /*
  * Bytes of device workspace attn_bwd needs: the delta vector
- * D_i = sum_c dO_ic O_ic (fp32 [B,H,N]), rounded up to 256 bytes.  Returns 0
- * for invalid sizes.
+ * D_i = sum_c dO_ic O_ic (fp32 [B,H,N]), rounded up to 256 bytes, and 256
+ * bytes of counters through which the kernels hand out their work.  Returns
+ * 0 for invalid sizes.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -164,7 +165,8 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *   dq, dk, dv       : [B,H,N,d] same dtype, written.
  *   workspace        : >= attn_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte
  *                      aligned, caller-owned; contents on entry are ignored
- *                      and on return are unspecified.
+ *                      and on return are unspecified.  Two calls in flight
+ *                      at once (on different streams) need two workspaces.
  * d in {64, 96, 128, 192, 256} (ATTN_ERR_UNSUPPORTED otherwise).  dK, dV
  * (per key tile; at d = 256 per key tile and half of the columns) and dQ (per
  * query tile) are each accumulated in fp32 by one CTA in a fixed order, so

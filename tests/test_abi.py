@@ -41,11 +41,11 @@ def test_status_strings_and_workspace_size_without_gpu(lib):
     assert lib.attn_status_string(4) == b"ATTN_ERR_TIMEOUT"
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     B, H, N, d = 2, 16, 8192, 128
-    want = B * H * N * 4  # the fp32 delta vector D, 256-byte multiple here
+    want = B * H * N * 4 + 256  # the fp32 delta vector D (a 256-byte multiple here), counters
     assert lib.attn_bwd_workspace_bytes(B, H, N, d) == want
     assert lib.attn_bwd_workspace_bytes(0, 1, 1, 128) == 0
     assert lib.attn_bwd_workspace_bytes(1, 1, 1, 80) == 0
-    assert lib.attn_bwd_workspace_bytes(1, 1, 3, 128) == 256  # rounded up
+    assert lib.attn_bwd_workspace_bytes(1, 1, 3, 128) == 512  # D rounded up, counters
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -1,12 +1,17 @@
 """Host model of the dQ kernel's coordination protocol (no GPU).
 
-The issuer meets the relay warp at a named barrier (no time limit) before
-each MMA group: per step j of a query tile, A (K_j, and at j = 0 Q / dO,
-have landed), B for j > 0 (dS_{j-1} is ready; at j = 1 also the previous
+Query tiles are handed out at run time: the producer takes the next one
+from a counter and publishes it in a ring of 4 entries (-1 after the last),
+which the relay (after waiting for the entry), the issuer (after meeting the
+relay at its named barrier, U), and the warpgroups read and release.  The
+issuer meets the relay warp at a named barrier (no time limit) before each
+MMA group: per tile U, then per step j of a query tile, A (K_j, and at
+j = 0 Q / dO, have landed), B for j > 0 (dS_{j-1} is ready; at j = 1 also the previous
 tile's dQ has been stored), C (V_j has landed and S_j has been read); per
 tile D (the last dS is ready).  The relay waits on the pipeline's mbarriers
-(bounded); after a wait runs out both warps still walk the whole schedule
-with the abort bit carried by the barrier, so every rendezvous pairs up.
+(bounded); after a wait runs out both warps still walk the rest of the
+tile's schedule with the abort bit carried by the barrier and leave together
+at the next U, so every rendezvous pairs up.
 The warpgroups and the producer use bounded mbarrier waits only and leave at
 their first failed wait.
 
@@ -27,6 +32,7 @@ WAIT_LIMIT_S = 0.05
 HANG_S = 3.0
 UNITS = [4, 1, 3, 2, 1, 5]  # steps (key tiles) of each query tile
 K_SLOTS, V_SLOTS = 3, 2
+UNIT_SLOTS = 4
 
 
 class Hang(Exception):
@@ -88,6 +94,10 @@ class CTA:
         self.s_full = [MBar(), MBar()]
         self.s_read, self.dp_full = MBar(2), MBar()
         self.ds_ready, self.dq_full, self.dq_free = MBar(2), MBar(), MBar(2)
+        self.unit_full = [MBar() for _ in range(UNIT_SLOTS)]
+        self.unit_empty = [MBar(4) for _ in range(UNIT_SLOTS)]  # issuer, relay, 2 warpgroups
+        self.ring = [None] * UNIT_SLOTS
+        self.next_unit = 0
         self.rv = Rendezvous()
         self.stored = 0
 
@@ -105,12 +115,38 @@ class CTA:
         return False
 
 
+def publish(c, un):
+    """Producer side of the unit ring: the next tile, or -1 after the last."""
+    us = un % UNIT_SLOTS
+    if not c.wait(c.unit_empty[us], ((un // UNIT_SLOTS) & 1) ^ 1):
+        return None
+    u = c.next_unit if c.next_unit < len(UNITS) else -1
+    c.next_unit += 1
+    c.ring[us] = u
+    c.unit_full[us].arrive()
+    return u
+
+
+def read(c, un):
+    us = un % UNIT_SLOTS
+    u = c.ring[us]
+    c.unit_empty[us].arrive()
+    return u
+
+
 def producer(c):
     k_it = v_it = 0
-    for u, n in enumerate(UNITS):
-        if not c.wait(c.q_empty, (u & 1) ^ 1):
+    un = q_it = 0
+    while True:
+        u = publish(c, un)
+        un += 1
+        if u is None or u < 0:
+            return
+        n = UNITS[u]
+        if not c.wait(c.q_empty, (q_it & 1) ^ 1):
             return
         c.q_full.arrive()
+        q_it += 1
         for _ in range(n):
             if not c.wait(c.k_empty[k_it % K_SLOTS], ((k_it // K_SLOTS) & 1) ^ 1):
                 return
@@ -125,7 +161,16 @@ def producer(c):
 def issuer(c):
     k_it = v_it = step = 0
     aborted = False
-    for n in UNITS:
+    un = 0
+    while True:
+        aborted = c.rv.go(aborted)                          # U
+        if aborted:
+            return
+        u = read(c, un)
+        un += 1
+        if u < 0:
+            return
+        n = UNITS[u]
         prev_ks = 0
         for j in range(n):
             ks, vs, sb = k_it % K_SLOTS, v_it % V_SLOTS, step & 1
@@ -155,24 +200,37 @@ def issuer(c):
 def relay(c):
     k_it = v_it = step = 0
     aborted = False
+    tile = 0  # tiles begun
 
     def wait(bar, parity):
         nonlocal aborted
         if not aborted:
             aborted = not c.wait(bar, parity)
 
-    for u, n in enumerate(UNITS):
+    un = 0
+    while True:
+        wait(c.unit_full[un % UNIT_SLOTS], (un // UNIT_SLOTS) & 1)
+        if aborted and c.early:
+            return
+        aborted = c.rv.go(aborted)                          # U
+        if aborted:
+            return
+        u = read(c, un)
+        un += 1
+        if u < 0:
+            return
+        n = UNITS[u]
         for j in range(n):
             if j == 0:
-                wait(c.q_full, u & 1)
+                wait(c.q_full, tile & 1)
             wait(c.k_full[k_it % K_SLOTS], (k_it // K_SLOTS) & 1)
             if aborted and c.early:
                 return
             aborted = c.rv.go(aborted)
             if j > 0:
                 wait(c.ds_ready, (step - 1) & 1)
-                if j == 1 and u > 0:
-                    wait(c.dq_free, (u - 1) & 1)
+                if j == 1 and tile > 0:
+                    wait(c.dq_free, (tile - 1) & 1)
                 aborted = c.rv.go(aborted)
             wait(c.v_full[v_it % V_SLOTS], (v_it // V_SLOTS) & 1)
             wait(c.s_read, step & 1)
@@ -181,15 +239,25 @@ def relay(c):
             v_it += 1
             step += 1
         wait(c.ds_ready, (step - 1) & 1)
-        if n == 1 and u > 0:
-            wait(c.dq_free, (u - 1) & 1)
+        if n == 1 and tile > 0:
+            wait(c.dq_free, (tile - 1) & 1)
         aborted = c.rv.go(aborted)
+        tile += 1
 
 
 def warpgroup(c):
     step = 0
-    for u, n in enumerate(UNITS):
-        for _ in range(n):
+    tile = 0
+    un = 0
+    while True:
+        us = un % UNIT_SLOTS
+        if not c.wait(c.unit_full[us], (un // UNIT_SLOTS) & 1):
+            return
+        u = read(c, un)
+        un += 1
+        if u < 0:
+            return
+        for _ in range(UNITS[u]):
             if not c.wait(c.s_full[step & 1], (step >> 1) & 1):
                 return
             c.s_read.arrive()
@@ -197,11 +265,12 @@ def warpgroup(c):
                 return
             c.ds_ready.arrive()
             step += 1
-        if not c.wait(c.dq_full, u & 1):
+        if not c.wait(c.dq_full, tile & 1):
             return
         with c.lock:
             c.stored += 1
         c.dq_free.arrive()
+        tile += 1
 
 
 def run(fail_p, seed, relay_leaves_early=False):
