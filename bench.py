@@ -52,7 +52,7 @@ LAUNCHES = {"fwd": 1, "bwd": 3, "quant": 3, "fwd_fp8": 1}  # kernels per compone
 KERNEL_SOURCES = {
     "fwd": ["fwd.cu", "fwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh"],
     "fwd_fp8": ["fwd.cu", "fwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh"],
-    "bwd": ["bwd.cu", "bwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh"],
+    "bwd": ["bwd.cu", "bwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh", "unit_ring.cuh"],
     "quant": ["fp8.cu", "fp8.cuh", "sm103_ptx.cuh"],
 }
 

@@ -416,6 +416,13 @@ attn_status bwd_wide_impl(DeviceInfo* di, const void* q, const void* k, const vo
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  p.sched = reinterpret_cast<int*>(static_cast<char*>(workspace) + bwd_delta_bytes(B, H, N));
+  // Only the dK/dV kernel's order is blocked by heads: blocking the wide dQ
+  // kernel's (K_j, V_j streamed 64 keys at a time) measured slower at d = 192
+  // (2.61 against 2.68 ms for the backward) and the same at d = 256.
+  const double head_bytes = (double)N * d * 4.0;  // two streamed 16-bit tensors of a head
+  p.head_block = bwd_head_block(head_bytes * p.group, p.BHkv);
+  p.head_block_q = p.BH;
   a.num_sms = di->num_sms;
   a.stream = static_cast<cudaStream_t>(stream);
   a.causal = causal != 0;

@@ -52,6 +52,7 @@
 #include "sm103_ptx.cuh"
 #include "smem_attr.cuh"
 #include "tiles.cuh"
+#include "unit_ring.cuh"
 
 namespace attn {
 
@@ -64,10 +65,6 @@ constexpr int kWarpRelay = 10;
 constexpr uint32_t kBarRelay = 3;  // named barrier: relay warp + issuer warp (64 threads)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStatusLayout = 5;  // shared memory not 1024-byte aligned
-// Unit ring: entries published by the producer; each is released by the
-// issuer, the relay and the 8 compute warps (one arrival each).
-constexpr int kUnitSlots = 4;
-constexpr int kUnitReaders = 10;
 // Bytes of a 128-row tile of 16-bit values with D columns (padded to a
 // multiple of 64).
 template <int D>
@@ -82,46 +79,6 @@ __device__ __forceinline__ uint32_t half_packed_col(int kk) {
 
 __device__ __forceinline__ uint32_t pack16x2(bool bf16, float lo, float hi) {
   return bf16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
-}
-
-// Producer side of the unit ring (one thread): once entry un's slot has been
-// released, takes the next unit from the counter and publishes it (-1 once
-// the counter has passed num_units).  Returns the unit, or -1 with ok false
-// when the wait ran out.
-__device__ __forceinline__ int publish_unit(volatile int* ring, uint32_t full0, uint32_t empty0,
-                                            uint32_t un, int* counter, int num_units,
-                                            const Watchdog& wd, bool& ok, int site) {
-  const uint32_t us = un % kUnitSlots;
-  ok = mbar_wait(empty0 + 8u * us, ((un / kUnitSlots) & 1) ^ 1, wd, site);
-  if (!ok) return -1;
-  int u = atomicAdd(counter, 1);
-  if (u >= num_units) u = -1;
-  ring[us] = u;
-  mbar_arrive(full0 + 8u * us);
-  return u;
-}
-
-// Reader side (every lane of a warp): waits for entry un, reads it and
-// releases it with one arrival for the warp.  Returns -1 with ok false when
-// the wait ran out.
-__device__ __forceinline__ int take_unit(volatile int* ring, uint32_t full0, uint32_t empty0,
-                                         uint32_t un, const Watchdog& wd, bool& ok, int site) {
-  const uint32_t us = un % kUnitSlots;
-  ok = mbar_wait(full0 + 8u * us, (un / kUnitSlots) & 1, wd, site);
-  const int u = ok ? ring[us] : -1;
-  __syncwarp();
-  if (ok && (threadIdx.x & 31) == 0) mbar_arrive(empty0 + 8u * us);
-  return u;
-}
-
-// The same for the relay / issuer pair: the relay has waited for entry un and
-// met the issuer at their named barrier, so both read it and release it.
-__device__ __forceinline__ int read_unit(volatile int* ring, uint32_t empty0, uint32_t un) {
-  const uint32_t us = un % kUnitSlots;
-  const int u = ring[us];
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(empty0 + 8u * us);
-  return u;
 }
 
 // Loads a 128 x D 16-bit tile (boxes of 64 columns; columns past D are
@@ -207,14 +164,10 @@ __device__ __forceinline__ DkvUnit decode_dkv_unit(int u, const BwdParams& p) {
   DkvUnit w;
   if (CAUSAL || p.cu_seqlens != nullptr) {
     // K/V tile j sees query tiles j..n-1: ascending j is longest first,
-    // within blocks of head_block heads (the last block may be smaller).
-    const int per_blk = p.head_block * p.n_kblocks;
-    const int blk = u / per_blk;
-    const int r = u - blk * per_blk;
-    const int h0 = blk * p.head_block;
-    const int hb = min(p.head_block, p.BHkv - h0);
-    w.j = r / hb;
-    w.bhkv = h0 + (r - w.j * hb);
+    // within blocks of head_block heads.
+    const BlockedUnit bu = blocked_unit(u, p.BHkv, p.head_block, p.n_kblocks, 1);
+    w.j = bu.cls;
+    w.bhkv = bu.head;
   } else {
     w.bhkv = u / p.n_kblocks;
     w.j = u - w.bhkv * p.n_kblocks;
@@ -733,15 +686,10 @@ __device__ __forceinline__ DqUnit decode_dq_unit(int u, const BwdParams& p) {
   DqUnit w;
   if (CAUSAL || p.cu_seqlens != nullptr) {
     // Query tile i sees key tiles 0..i: descending i is longest first,
-    // within blocks of head_block_q heads (the last block may be smaller).
-    const int per_blk = p.head_block_q * p.n_qtiles;
-    const int blk = u / per_blk;
-    const int r0 = u - blk * per_blk;
-    const int h0 = blk * p.head_block_q;
-    const int hb = min(p.head_block_q, p.BH - h0);
-    const int r = r0 / hb;
-    w.bh = h0 + (r0 - r * hb);
-    w.i = p.n_qtiles - 1 - r;
+    // within blocks of head_block_q heads.
+    const BlockedUnit bu = blocked_unit(u, p.BH, p.head_block_q, p.n_qtiles, 1);
+    w.bh = bu.head;
+    w.i = p.n_qtiles - 1 - bu.cls;
   } else {
     w.bh = u / p.n_qtiles;
     w.i = u - w.bh * p.n_qtiles;

@@ -38,6 +38,7 @@
 #include "bwd.cuh"
 #include "sm103_ptx.cuh"
 #include "smem_attr.cuh"
+#include "unit_ring.cuh"
 #include "tiles.cuh"
 
 namespace attn {
@@ -104,10 +105,11 @@ struct WDkvLayout {
   static constexpr int kBar = kVec0 + kRing * 512;
   enum {
     kKvFull, kKvEmpty, kFull, kEmpty = kFull + kRing, kSFull = kEmpty + kRing, kDpFull,
-    kPReady, kDsReady, kDkvFull, kDkvFree, kDrain, kNumBars
+    kPReady, kDsReady, kDkvFull, kDkvFree, kDrain, kUnitFull,
+    kUnitEmpty = kUnitFull + kUnitSlots, kNumBars = kUnitEmpty + kUnitSlots
   };
-  static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM address, abort flag, unit ring
+  static constexpr int kBytes = kMisc + 16 + 4 * kUnitSlots;
   static_assert(kItem == 2 * kBox128 || !kKt, "a K half must fill one ring slot");
   static_assert(kBytes <= 232448, "shared memory budget (227 KB) exceeded");
   // tensor memory
@@ -131,12 +133,13 @@ __device__ __forceinline__ WDkvUnit decode_wdkv(int u, const BwdParams& p) {
   WDkvUnit w;
   int bhkv;
   if (CAUSAL) {
-    // Key tile j sees query sub-tiles 2j..: ascending j is longest first.
-    const int per_j = p.BHkv * L::kHalves;
-    w.j = u / per_j;
-    const int r = u - w.j * per_j;
-    bhkv = r / L::kHalves;
-    w.h = r - bhkv * L::kHalves;
+    // Key tile j sees query sub-tiles 2j..: ascending j is longest first,
+    // within blocks of head_block heads (both column halves of a key tile
+    // are neighbours).
+    const BlockedUnit bu = blocked_unit(u, p.BHkv, p.head_block, p.n_kblocks, L::kHalves);
+    w.j = bu.cls;
+    bhkv = bu.head;
+    w.h = bu.inner;
   } else {
     const int per_kv = p.n_kblocks * L::kHalves;
     bhkv = u / per_kv;
@@ -181,12 +184,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto slot_addr = [&](uint32_t it) { return sbase + L::kRing0 + (it % kRing) * L::kItem; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   Watchdog wd{p.status, abort_flag, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(bar(L::kUnitFull + s), 1);
+      mbar_init(bar(L::kUnitEmpty + s), kUnitReaders);
+    }
     mbar_init(bar(L::kKvFull), 1);
     mbar_init(bar(L::kKvEmpty), 1);
     for (int s = 0; s < kRing; ++s) {
@@ -210,8 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
-  const int G = gridDim.x;
-  const int cta = blockIdx.x;
   const int num_units = p.BHkv * p.n_kblocks * L::kHalves;
 
   if (warp == kWarpProducer) {
@@ -232,9 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       return ok;
     };
-    for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    uint32_t un = 0;
+    while (ok) {
+      int u = -1;
+      if (lane == 0)
+        u = publish_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un, p.sched, num_units,
+                         wd, ok, 38);
+      ++un;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!ok || u < 0) break;
       const WDkvUnit w = decode_wdkv<D, CAUSAL>(u, p);
       if (lane == 0) {
         ok = mbar_wait(bar(L::kKvEmpty), (kv_it & 1) ^ 1, wd, 21);
@@ -345,9 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(L::kEmpty + qpos % kRing));
       mma_commit(bar(L::kEmpty + dpos % kRing));
     };
-    for (int k = 0;; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    for (uint32_t un = 0;; ++un) {
+      // the relay has seen the next unit published (after an abort both
+      // warps leave here, having met at every rendezvous so far)
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      if (aborted) break;
+      const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+      if (u < 0) break;
       const WDkvUnit w = decode_wdkv<D, CAUSAL>(u, p);
       const uint32_t kpos = it;
       if constexpr (L::kKt) it += 2;
@@ -443,9 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_slot = [&](uint32_t pos, int site) {
       wait_all(bar(L::kFull + pos % kRing), (pos / kRing) & 1, site);
     };
-    for (int k = 0;; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    for (uint32_t un = 0;; ++un) {
+      wait_all(bar(L::kUnitFull + un % kUnitSlots), (un / kUnitSlots) & 1, 39);
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      if (aborted) break;
+      const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+      if (u < 0) break;
       const WDkvUnit w = decode_wdkv<D, CAUSAL>(u, p);
       wait_all(bar(L::kKvFull), kv_it & 1, 25);
       ++kv_it;
@@ -483,11 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = tbase + lane_base + L::kColS + 32 * wg;
     const uint32_t dp_addr = tbase + lane_base + L::kColDP + 32 * wg;
     const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
-    uint32_t it = 0, st_it = 0, unit_it = 0;
+    uint32_t it = 0, st_it = 0, unit_it = 0, un = 0;
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    while (ok) {
+      const int u = take_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un++, wd, ok, 40);
+      ok = named_bar_and(1 + wg, 128, ok);
+      if (!ok || u < 0) break;
       const WDkvUnit w = decode_wdkv<D, CAUSAL>(u, p);
       if constexpr (L::kKt) it += 2;
       const int key = w.j * 128 + r;
@@ -627,10 +648,11 @@ struct WDqLayout {
   static constexpr int kBar = kRing0 + kRing * kItem;
   enum {
     kQFull, kQEmpty, kDoFull, kDoEmpty, kFull, kEmpty = kFull + kRing, kSFull = kEmpty + kRing,
-    kSRead = kSFull + 2, kDpFull, kDsReady, kDqFull, kDqFree, kDrain, kNumBars
+    kSRead = kSFull + 2, kDpFull, kDsReady, kDqFull, kDqFree, kDrain, kUnitFull,
+    kUnitEmpty = kUnitFull + kUnitSlots, kNumBars = kUnitEmpty + kUnitSlots
   };
-  static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM address, abort flag, unit ring
+  static constexpr int kBytes = kMisc + 16 + 4 * kUnitSlots;
   static_assert(kItem == 2 * kBox128 || !kQRing, "a Q half must fill one ring slot");
   static_assert(kBytes <= 232448, "shared memory budget (227 KB) exceeded");
   // tensor memory: dQ, two 64-column step buffers, Q (and dO) as 16-bit pairs
@@ -648,10 +670,11 @@ template <bool CAUSAL>
 __device__ __forceinline__ WDqUnit decode_wdq(int u, const BwdParams& p) {
   WDqUnit w;
   if (CAUSAL) {
-    // Query tile i sees key sub-tiles 0..2i+1: descending i is longest first.
-    const int r = u / p.BH;
-    w.bh = u - r * p.BH;
-    w.i = p.n_qtiles - 1 - r;
+    // Query tile i sees key sub-tiles 0..2i+1: descending i is longest first,
+    // within blocks of head_block_q heads.
+    const BlockedUnit bu = blocked_unit(u, p.BH, p.head_block_q, p.n_qtiles, 1);
+    w.bh = bu.head;
+    w.i = p.n_qtiles - 1 - bu.cls;
   } else {
     w.bh = u / p.n_qtiles;
     w.i = u - w.bh * p.n_qtiles;
@@ -683,12 +706,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto slot_addr = [&](uint32_t it) { return sbase + L::kRing0 + (it % kRing) * L::kItem; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   Watchdog wd{p.status, abort_flag, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(bar(L::kUnitFull + s), 1);
+      mbar_init(bar(L::kUnitEmpty + s), kUnitReaders);
+    }
     mbar_init(bar(L::kQFull), 1);
     mbar_init(bar(L::kQEmpty), 1);
     mbar_init(bar(L::kDoFull), 1);
@@ -714,8 +742,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
-  const int G = gridDim.x;
-  const int cta = blockIdx.x;
   const int num_units = p.BH * p.n_qtiles;
 
   if (warp == kWarpProducer) {
@@ -731,9 +757,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar(L::kEmpty + it % kRing), ((it / kRing) & 1) ^ 1, wd, 42);
         return ok;
       };
-      for (int k = 0; ok; ++k) {
-        const int u = snake_unit(k, cta, G);
-        if (u >= num_units) break;
+      uint32_t un = 0;
+      while (ok) {
+        const int u = publish_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un++,
+                                   p.sched + 1, num_units, wd, ok, 38);
+        if (u < 0) break;
         const WDqUnit w = decode_wdq<CAUSAL>(u, p);
         if constexpr (L::kQRing) {
           for (int half = 0; half < 2 && ok; ++half) {
@@ -809,9 +837,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    desc_plus(kmn, mnmajor16_off(kk)), kIdQ, kk > 0 ? 1u : acc0);
       mma_commit(bar(L::kEmpty + kpos % kRing));
     };
-    for (int k = 0;; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    for (uint32_t un = 0;; ++un) {
+      // the relay has seen the next unit published (after an abort both
+      // warps leave here, having met at every rendezvous so far)
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      if (aborted) break;
+      const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+      if (u < 0) break;
       const WDqUnit w = decode_wdq<CAUSAL>(u, p);
       const uint32_t qpos = it;
       if constexpr (L::kQRing) it += 2;
@@ -910,9 +942,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_slot = [&](uint32_t pos, int site) {
       wait_all(bar(L::kFull + pos % kRing), (pos / kRing) & 1, site);
     };
-    for (int k = 0;; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    for (uint32_t un = 0;; ++un) {
+      wait_all(bar(L::kUnitFull + un % kUnitSlots), (un / kUnitSlots) & 1, 39);
+      aborted = named_bar_or(kBarRelay, 64, aborted);
+      if (aborted) break;
+      const int u = read_unit(unit_ring, bar(L::kUnitEmpty), un);
+      if (u < 0) break;
       const WDqUnit w = decode_wdq<CAUSAL>(u, p);
       const uint32_t qpos = it;
       if constexpr (L::kQRing) it += 2;
@@ -952,11 +987,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t dq_addr = tbase + lane_base + L::kColDQ;
     const float sl2 = p.scale_log2;
-    uint32_t unit_it = 0, step_it = 0;
+    uint32_t unit_it = 0, step_it = 0, un = 0;
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int u = snake_unit(k, cta, G);
-      if (u >= num_units) break;
+    while (ok) {
+      const int u = take_unit(unit_ring, bar(L::kUnitFull), bar(L::kUnitEmpty), un++, wd, ok, 40);
+      ok = named_bar_and(1 + wg, 128, ok);
+      if (!ok || u < 0) break;
       const WDqUnit w = decode_wdq<CAUSAL>(u, p);
       const int row = w.i * 128 + r;
       const bool in = row < p.N;

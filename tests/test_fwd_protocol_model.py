@@ -51,14 +51,19 @@ class Rendezvous:
 
 
 class MBar:
-    def __init__(self):
-        self.phase = 0
+    """mbarrier: a phase completes after `count` arrivals."""
+
+    def __init__(self, count=1):
+        self.count, self.pending, self.phase = count, count, 0
         self.cv = threading.Condition()
 
     def arrive(self):
         with self.cv:
-            self.phase += 1
-            self.cv.notify_all()
+            self.pending -= 1
+            if self.pending == 0:
+                self.pending = self.count
+                self.phase += 1
+                self.cv.notify_all()
 
     def done(self, parity):
         return (self.phase & 1) != parity

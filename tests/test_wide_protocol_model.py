@@ -8,7 +8,9 @@ roles as threads with the kernels' loop structure -- the forward's one query
 tile per unit with two S buffers, its K/V chunk ring in consumption order
 (K0 K1 V0 K2 V1 ...) and its P V completion barrier waited only on a rescale;
 the backward's dK/dV kernel (64-row Q/dO items through a ring, the unit's K
-halves through the same ring) and dQ kernel (Q halves and K_j/V_j items) --
+halves through the same ring, units handed out at run time through a
+4-entry ring after which the relay and issuer leave together at the next
+unit's rendezvous once aborted) and dQ kernel (Q halves and K_j/V_j items) --
 with named barriers as OR-reducing rendezvous and mbarriers as phase counters
 whose waits fail at randomly injected points, and check that no injected
 failure leaves a role blocked, that a clean run completes every epilogue,
@@ -253,6 +255,7 @@ def test_wide_forward_model_catches_softmax_that_leaves_early():
 
 BWD_UNITS = [4, 1, 3, 2, 5]  # steps of each unit
 R = 5                        # ring slots
+UNIT_SLOTS = 4               # unit ring entries
 
 
 class Bwd(Ctx):
@@ -267,11 +270,38 @@ class Bwd(Ctx):
         self.pready, self.dsready = MBar(), MBar()
         self.outfull, self.outfree = MBar(), MBar()
         self.relay_bar = Rendezvous("kBarRelay")
+        self.unit_full = [MBar() for _ in range(UNIT_SLOTS)]
+        self.unit_empty = [MBar(3) for _ in range(UNIT_SLOTS)]  # relay, issuer, compute
+        self.ring_units = [None] * UNIT_SLOTS
+        self.next_unit = 0
+
+
+def bwd_publish(c, un):
+    us = un % UNIT_SLOTS
+    if not c.wait(c.unit_empty[us], ((un // UNIT_SLOTS) & 1) ^ 1):
+        return None
+    u = c.next_unit if c.next_unit < len(BWD_UNITS) else -1
+    c.next_unit += 1
+    c.ring_units[us] = u
+    c.unit_full[us].arrive()
+    return u
+
+
+def bwd_read_unit(c, un):
+    us = un % UNIT_SLOTS
+    u = c.ring_units[us]
+    c.unit_empty[us].arrive()
+    return u
 
 
 def bwd_producer(c):
-    it = unit_it = 0
-    for steps in BWD_UNITS:
+    it = unit_it = un = 0
+    while True:
+        u = bwd_publish(c, un)
+        un += 1
+        if u is None or u < 0:
+            return
+        steps = BWD_UNITS[u]
         if not c.wait(c.tileempty, (unit_it & 1) ^ 1):
             return
         c.tilefull.arrive()
@@ -292,7 +322,17 @@ def bwd_relay(c):
         if not aborted:
             aborted = not c.wait(bar, par)
 
-    for steps in BWD_UNITS:
+    un = 0
+    while True:
+        wait_all(c.unit_full[un % UNIT_SLOTS], (un // UNIT_SLOTS) & 1)
+        aborted = c.relay_bar.go(aborted)
+        if aborted:
+            return
+        u = bwd_read_unit(c, un)
+        un += 1
+        if u < 0:
+            return
+        steps = BWD_UNITS[u]
         wait_all(c.tilefull, unit_it & 1)
         for _ in range(c.k_halves):
             wait_all(c.full[it % R], (it // R) & 1)
@@ -319,9 +359,17 @@ def bwd_relay(c):
 
 
 def bwd_issuer(c):
-    it = 0
+    it = un = 0
     aborted = False
-    for steps in BWD_UNITS:
+    while True:
+        aborted = c.relay_bar.go(aborted)
+        if aborted:
+            return
+        u = bwd_read_unit(c, un)
+        un += 1
+        if u < 0:
+            return
+        steps = BWD_UNITS[u]
         kpos = it
         it += c.k_halves
         prev = None
@@ -354,8 +402,15 @@ def bwd_issuer(c):
 
 
 def bwd_compute(c):
-    st_it = unit_it = 0
-    for steps in BWD_UNITS:
+    st_it = unit_it = un = 0
+    while True:
+        if not c.wait(c.unit_full[un % UNIT_SLOTS], (un // UNIT_SLOTS) & 1):
+            return
+        u = bwd_read_unit(c, un)
+        un += 1
+        if u < 0:
+            return
+        steps = BWD_UNITS[u]
         for _ in range(steps):
             par = st_it & 1
             if not c.wait(c.sfull, par):
