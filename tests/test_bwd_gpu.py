@@ -147,3 +147,46 @@ def test_backward_is_deterministic(attn_lib, causal):
     assert attn_lib.poll_status() == (0, 0)
     for a, b in zip(g1, g2):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_workspace_contents_do_not_matter(attn_lib, d):
+    """The kernels take their units from counters in the workspace, which the
+    D pass zeroes first: a workspace full of 0xFF bytes gives the same bits as
+    a zeroed one."""
+    w = wl.Workload("ws", "bwd", 1, 4, 1100, d, "bf16", True, seed=31)
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = attn_lib.fwd(q, k, v, causal=True)
+    nbytes = attn_lib.bwd_workspace_bytes(1, 4, 1100, d)
+    ws0 = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    ws1 = torch.full((nbytes,), 255, dtype=torch.uint8, device="cuda")
+    g0 = attn_lib.bwd(q, k, v, o, do, lse, causal=True, workspace=ws0)
+    g1 = attn_lib.bwd(q, k, v, o, do, lse, causal=True, workspace=ws1)
+    assert attn_lib.poll_status() == (0, 0)
+    for a, b in zip(g0, g1):
+        assert torch.isfinite(a).all()
+        assert torch.equal(a, b)
+
+
+def test_two_streams_with_their_own_workspaces(attn_lib):
+    """Two backward calls in flight at once on two streams, each with its own
+    workspace (and so its own work counters), match a call run alone."""
+    w = wl.Workload("streams", "bwd", 2, 4, 2048, 128, "bf16", True, seed=33)
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = attn_lib.fwd(q, k, v, causal=True)
+    ref = attn_lib.bwd(q, k, v, o, do, lse, causal=True)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for s in streams:
+        with torch.cuda.stream(s):
+            outs.append(attn_lib.bwd(q, k, v, o, do, lse, causal=True))
+    torch.cuda.synchronize()
+    assert attn_lib.poll_status() == (0, 0)
+    for g in outs:
+        for a, b in zip(g, ref):
+            assert torch.equal(a, b)
