@@ -243,15 +243,15 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
  * loops that must not call cudaMalloc (which can synchronise the device) on
  * the request path, or programs with a fixed memory plan.  It computes the
  * same dQ, dK, dV as attn_bwd, with the same arguments minus the workspace;
- * the scratch (the fp32 delta vector) lives in a fixed device array inside
- * the library.
+ * the scratch (the fp32 delta vector and the kernels' work counters) lives
+ * in a fixed device array inside the library.
  *   Limit: B*H*N <= 4194304 query rows and d in {64, 96, 128, 192, 256}; larger
  *   problems return ATTN_ERR_INVALID_ARG, other head dims ATTN_ERR_UNSUPPORTED.
  *   Memory: the array (16 MB) is part of the library image and is held on
  *   every GPU that loads the library until the process exits.
  *   Sharing: all calls use the same array: calls that overlap on the GPU
  *   (different streams, or different host threads, without ordering between
- *   them) race on it.
+ *   them) race on it and give wrong results.
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress) with that device current; make that
  *   first call before any stream capture.  The address is kept for the
