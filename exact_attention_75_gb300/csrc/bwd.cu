@@ -114,7 +114,7 @@ struct DkvLayout {
   enum {
     kKvFull, kKvEmpty, kQFull, kQEmpty = kQFull + kQSlots, kDoFull = kQEmpty + kQSlots,
     kDoEmpty = kDoFull + kDoSlots, kVecEmpty = kDoEmpty + kDoSlots,
-    kSFull = kVecEmpty + kDoSlots, kDpFull, kPReady, kDsReady,
+    kSFull = kVecEmpty + kDoSlots, kDpFull = kSFull + 2, kPReady, kDsReady = kPReady + 2,
     kDkvFull, kDkvFree, kDrain, kUnitFull, kUnitEmpty = kUnitFull + kUnitSlots,
     kNumBars = kUnitEmpty + kUnitSlots
   };
@@ -125,8 +125,17 @@ struct DkvLayout {
 
 // Tensor memory: dV [0,128)  dK [128,256)  S^T [256,384)  dP^T [384,512).
 // P^T (16-bit) of warpgroup h overwrites S^T columns [256+64h, 256+64h+32),
-// dS^T those of dP^T.
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+// dS^T those of dP^T.  At d = 64 dV and dK take 64 columns each, which leaves
+// room for a second S^T buffer: dV [0,64)  dK [64,128)  S^T [128,256) and
+// [256,384) by step parity  dP^T [384,512); S^T(s+1) can then be issued
+// before dV(s) has read P^T(s).
+constexpr uint32_t kColDV = 0, kColDP = 384;
+template <int D>
+constexpr bool kDoubleS = kPaddedD<D> == 64;
+template <int D>
+constexpr uint32_t kColDK = kDoubleS<D> ? 64 : 128;
+template <int D>
+constexpr uint32_t kColST0 = kDoubleS<D> ? 128 : 256;
 
 // Rows of sequence b: [row0, row0 + len) of every head.  Dense batches are
 // one sequence of N rows per (batch, head) tensor-map index.
@@ -232,8 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kVecEmpty + s), 8);  // one arrival per compute warp
     }
     mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kSFull + 1), 1);
     mbar_init(bar(L::kDpFull), 1);
     mbar_init(bar(L::kPReady), 256);
+    mbar_init(bar(L::kPReady + 1), 256);
     mbar_init(bar(L::kDsReady), 256);
     mbar_init(bar(L::kDkvFull), 1);
     mbar_init(bar(L::kDkvFree), 256);
@@ -361,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qd_mn = mnmajor_base(sbase + L::kQ0 + qs * kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ts(tbase + kColDK, tbase + kColDP + half_packed_col(kk),
+          mma_f16_ts(tbase + kColDK<D>, tbase + kColDP + half_packed_col(kk),
                      desc_plus(qd_mn, mnmajor16_off(kk)), kIdKV, kk > 0 ? 1u : acc0);
         mma_commit(bar(L::kQEmpty + qs));
       };
@@ -374,20 +385,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u < 0) break;
         const DkvUnit w = decode_dkv_unit<CAUSAL>(u, p);
         if (w.nsteps == 0) continue;
-        for (int s = 0; s < w.nsteps; ++s) {
-          const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
-          // Q_i(s) (and at s = 0 the unit's K, V) have landed.
-          // S^T = K Q_i^T (the previous P^T was consumed by the previous dV,
-          // and its S^T read before that P^T was handed over)
+        // S^T(step) = K Q_i^T into its buffer (the P^T last held there was
+        // consumed by a dV issued before, and its S^T read before that P^T
+        // was handed over)
+        auto issue_st = [&](uint32_t step) {
+          const uint32_t b = kDoubleS<D> ? (step & 1) : 0;
+          const uint64_t qd = kmajor_base(sbase + L::kQ0 + (step % L::kQSlots) * kTile);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16_ss(tbase + kColST0<D> + 128 * b, desc_plus(kd_k, kmajor16_off(kk)),
+                       desc_plus(qd, kmajor16_off(kk)), kIdS, kk > 0);
+          mma_commit(bar(L::kSFull + b));
+        };
+        if constexpr (kDoubleS<D>) {
+          // Q_i(0) and the unit's K, V have landed: S^T(0)
           aborted = named_bar_or(kBarRelay, 64, aborted);
           if (!aborted && lane == 0) {
             tc_fence_after();
-            const uint64_t qd = kmajor_base(sbase + L::kQ0 + qs * kTile);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_f16_ss(tbase + kColS, desc_plus(kd_k, kmajor16_off(kk)),
-                         desc_plus(qd, kmajor16_off(kk)), kIdS, kk > 0);
-            mma_commit(bar(L::kSFull));
+            issue_st(st_it);
+          }
+        }
+        for (int s = 0; s < w.nsteps; ++s) {
+          const uint32_t ds = st_it % L::kDoSlots;
+          const uint32_t sbuf = kDoubleS<D> ? (st_it & 1) : 0;
+          if constexpr (!kDoubleS<D>) {
+            // Q_i(s) (and at s = 0 the unit's K, V) have landed: S^T(s)
+            aborted = named_bar_or(kBarRelay, 64, aborted);
+            if (!aborted && lane == 0) {
+              tc_fence_after();
+              issue_st(st_it);
+            }
           }
           // dK(s-1): its dS^T is in tensor memory
           if (s > 0) {
@@ -410,6 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                          desc_plus(dod, kmajor16_off(kk)), kIdS, kk > 0);
             mma_commit(bar(L::kDpFull));
           }
+          if constexpr (kDoubleS<D>) {
+            // Q_i(s+1) has landed: S^T(s+1) into the other buffer, ahead of dV(s)
+            if (s + 1 < w.nsteps) {
+              aborted = named_bar_or(kBarRelay, 64, aborted);
+              if (!aborted && lane == 0) {
+                tc_fence_after();
+                issue_st(st_it + 1);
+              }
+            }
+          }
           // dV += P^T dO_i (A = P^T from tensor memory) once P^T is there
           // (and, at s = 0, the previous unit's dV / dK have been stored)
           aborted = named_bar_or(kBarRelay, 64, aborted);
@@ -418,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dod_mn = mnmajor_base(doaddr);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ts(tbase + kColDV, tbase + kColS + half_packed_col(kk),
+              mma_f16_ts(tbase + kColDV, tbase + kColST0<D> + 128 * sbuf + half_packed_col(kk),
                          desc_plus(dod_mn, mnmajor16_off(kk)), kIdKV, kk > 0 || s > 0 ? 1u : 0u);
             mma_commit(bar(L::kDoEmpty + ds));  // dV(s) was the last reader of dO_i
           }
@@ -463,19 +500,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.nsteps == 0) continue;
       wait_all(bar(L::kKvFull), kv_it & 1, 25);
       ++kv_it;
+      if constexpr (kDoubleS<D>) {
+        wait_all(bar(L::kQFull + st_it % L::kQSlots), (st_it / L::kQSlots) & 1, 26);
+        aborted = named_bar_or(kBarRelay, 64, aborted);  // S^T(0)
+      }
       for (int s = 0; s < w.nsteps; ++s) {
         const uint32_t qs = st_it % L::kQSlots, ds = st_it % L::kDoSlots;
         const uint32_t par = st_it & 1;
-        wait_all(bar(L::kQFull + qs), (st_it / L::kQSlots) & 1, 26);
-        aborted = named_bar_or(kBarRelay, 64, aborted);
+        if constexpr (!kDoubleS<D>) {
+          wait_all(bar(L::kQFull + qs), (st_it / L::kQSlots) & 1, 26);
+          aborted = named_bar_or(kBarRelay, 64, aborted);
+        }
         if (s > 0) {
           wait_all(bar(L::kDsReady), par ^ 1, 27);
           aborted = named_bar_or(kBarRelay, 64, aborted);
         }
         wait_all(bar(L::kDoFull + ds), (st_it / L::kDoSlots) & 1, 28);
         aborted = named_bar_or(kBarRelay, 64, aborted);
+        if constexpr (kDoubleS<D>) {
+          if (s + 1 < w.nsteps) {
+            const uint32_t n1 = st_it + 1;
+            wait_all(bar(L::kQFull + n1 % L::kQSlots), (n1 / L::kQSlots) & 1, 26);
+            aborted = named_bar_or(kBarRelay, 64, aborted);  // S^T(s+1)
+          }
+        }
         if (s == 0 && unit_it > 0) wait_all(bar(L::kDkvFree), (unit_it - 1) & 1, 29);
-        wait_all(bar(L::kPReady), par, 30);
+        // with two S^T buffers P^T(s+1) can be handed over before this wait,
+        // so the hand-off barrier alternates with the buffer too
+        if constexpr (kDoubleS<D>)
+          wait_all(bar(L::kPReady + (st_it & 1)), (st_it >> 1) & 1, 30);
+        else
+          wait_all(bar(L::kPReady), par, 30);
         aborted = named_bar_or(kBarRelay, 64, aborted);
         ++st_it;
       }
@@ -488,7 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;                 // query half of every step
     const int r = threadIdx.x & 127;         // TMEM lane: key row
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tbase + lane_base + kColS + 64 * h;
     const uint32_t dp_addr = tbase + lane_base + kColDP + 64 * h;
     const float sl2 = p.scale_log2;
     uint32_t st_it = 0, unit_it = 0, un = 0;
@@ -505,7 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)zq;
         const uint32_t ds = st_it % L::kDoSlots;
         const uint32_t par = st_it & 1;
-        ok = mbar_wait(bar(L::kSFull), par, wd, 33);
+        const uint32_t sbuf = kDoubleS<D> ? (st_it & 1) : 0;
+        const uint32_t s_addr = tbase + lane_base + kColST0<D> + 128 * sbuf + 64 * h;
+        ok = mbar_wait(bar(L::kSFull + sbuf), kDoubleS<D> ? ((st_it >> 1) & 1) : par, wd, 33);
         // dO_i's full barrier also waits for the -LSE / -D vectors' writer
         ok = ok && mbar_wait(bar(L::kDoFull + ds), (st_it / L::kDoSlots) & 1, wd, 34);
         // Exit decisions are uniform over the warpgroup (its warps meet at
@@ -559,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(L::kPReady));
+        mbar_arrive(bar(L::kPReady + sbuf));
         // ---- dS^T = P^T o (dP^T - D)
         ok = mbar_wait(bar(L::kDpFull), par, wd, 35);
         ok = named_bar_and(1 + h, 128, ok);
@@ -609,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++unit_it;
       tc_fence_after();
       const int key = w.j * 128 + r;
-      const uint32_t src = tbase + lane_base + (h == 0 ? kColDV : kColDK);
+      const uint32_t src = tbase + lane_base + (h == 0 ? kColDV : kColDK<D>);
       const float mult = (h == 0) ? 1.f : p.scale;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(h == 0 ? p.dv : p.dk) +
                                             ((size_t)w.zkv * p.N + w.row0 + key) * D);

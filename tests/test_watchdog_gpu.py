@@ -68,15 +68,19 @@ def test_forward_winds_down_when_waits_run_out(attn_lib, dtype, d):
     assert np.max(np.abs(to64(lse[1, 2])[rows] - L_ref)) <= 5e-3
 
 
-def test_backward_winds_down_when_waits_run_out(attn_lib):
-    """The same for the backward main kernel: with a 1 us wait limit its roles
-    walk their schedules to the end without waiting, the launch reports
-    ATTN_ERR_TIMEOUT, and a following
-    backward at the normal limit matches the oracle."""
+@pytest.mark.parametrize("d", [128, 64])
+def test_backward_winds_down_when_waits_run_out(attn_lib, d):
+    """The same for the backward main kernels: with a 1 us wait limit their
+    roles walk their schedules to the end without waiting, the launch reports
+    ATTN_ERR_TIMEOUT, and a following backward at the normal limit matches
+    the oracle (d = 64 runs the dK/dV kernel with two S^T buffers)."""
     import numpy as np
     import oracle
     from helpers import to64
-    w = wl.Workload("t", "bwd", 1, 2, 1024, 128, "bf16", True, seed=11)
+    # at d = 64 the small case's waits are all shorter than the limit; a
+    # larger one gives every CTA several units, so some producer waits
+    H, N = (2, 1024) if d == 128 else (8, 4096)
+    w = wl.Workload("t", "bwd", 1, H, N, d, "bf16", True, seed=11)
     inp = wl.make_inputs(w)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
     o, lse = attn_lib.fwd(q, k, v, causal=True)
@@ -84,10 +88,13 @@ def test_backward_winds_down_when_waits_run_out(attn_lib):
     _expect_timeout(attn_lib, lambda: attn_lib.bwd(q, k, v, o, do, lse, causal=True))
     dq, dk, dv = attn_lib.bwd(q, k, v, o, do, lse, causal=True)
     assert attn_lib.poll_status() == (0, 0)
+    heads = [(0, 0), (0, H - 1)]
     refs = oracle.attention_backward(*(to64(inp[n]) for n in ("q", "k", "v", "do")), True,
-                                     w.scale)
+                                     w.scale, heads=heads)
     for g, r in zip((dq, dk, dv), refs):
-        assert np.max(np.abs(to64(g) - r)) <= 5e-2 * np.max(np.abs(r))
+        g = np.stack([to64(g)[b, h] for b, h in heads])
+        r = np.stack([r[b, h] for b, h in heads])
+        assert np.max(np.abs(g - r)) <= 5e-2 * np.max(np.abs(r))
 
 
 @pytest.mark.parametrize("d", [192, 256])
