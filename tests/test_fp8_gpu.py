@@ -46,6 +46,22 @@ def test_quantize_bit_exact_without_rotation(attn_lib, d, N):
         assert np.array_equal(codes_t, np.swapaxes(ref["codes"], 2, 3))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_quantize_many_blocks(attn_lib, d):
+    """2048 blocks of 64 rows, more than the GPU holds at once, with a ragged
+    32-row block ending every head: codes and scales bit-exact in both
+    layouts."""
+    w = wl.Workload("qm", "fwd_fp8", 2, 16, 4064, d, "bf16", False, outliers=True, seed=7 + d)
+    x = wl.make_inputs(w)["q"]
+    ref = oracle.quantize_blocks(to64(x), 64)
+    codes, scales = _quant(attn_lib, x)
+    assert np.array_equal(scales.view(np.uint32), ref["scales"].view(np.uint32))
+    assert np.array_equal(codes, ref["codes"])
+    codes_t, scales_t = _quant(attn_lib, x, transposed=True)
+    assert np.array_equal(scales_t, scales)
+    assert np.array_equal(codes_t, np.swapaxes(ref["codes"], 2, 3))
+
+
 def test_quantize_all_zero_block(attn_lib):
     x = torch.zeros((1, 1, 130, 128), dtype=torch.bfloat16)
     x[0, 0, 128:] = 1.0
