@@ -11,9 +11,11 @@
 //
 // d/8 lanes per row (8 values, one 16-byte read of each split's row per
 // lane), so a warp merges 32/(d/8) rows at once (rounded down: at d = 96
-// lanes 24-31 idle); the splits' rows are read
-// four at a time so their loads are in flight together; grid-stride over
-// rows; arithmetic in fp32.
+// lanes 24-31 idle).  One pass over the splits, four at a time (their LSE
+// and O reads in flight together): the running maximum m rises with each
+// group and the sums gathered so far are scaled by exp(m_old - m_new), as in
+// the online softmax, so no separate pass over the LSEs waits on memory
+// first; grid-stride over rows; arithmetic in fp32.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -58,32 +60,41 @@ __global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__
     const long row = row0 + sub;
     const bool live = sub < kRowsPerWarp && row < rows;
     const long rrow = live ? row : rows - 1;  // in-range address for idle lanes
-    float m = -INFINITY;
-    for (int s = 0; s < n_split; ++s) m = fmaxf(m, lse_part[(size_t)s * rows + rrow]);
+    float m = -INFINITY;  // the largest LSE_s so far
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     float l = 0.f;
-    if (m != -INFINITY) {
-      for (int s0 = 0; s0 < n_split; s0 += kBatch) {
-        uint4 w[kBatch];
-        float ls[kBatch];
+    for (int s0 = 0; s0 < n_split; s0 += kBatch) {
+      uint4 w[kBatch];
+      float ls[kBatch];
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int sk = min(s0 + k, n_split - 1);
-          ls[k] = s0 + k < n_split ? lse_part[(size_t)sk * rows + rrow] : -INFINITY;
-          w[k] = *reinterpret_cast<const uint4*>(o_part + ((size_t)sk * rows + rrow) * D + col);
-        }
+      for (int k = 0; k < kBatch; ++k) {
+        const int sk = min(s0 + k, n_split - 1);
+        ls[k] = s0 + k < n_split ? lse_part[(size_t)sk * rows + rrow] : -INFINITY;
+        w[k] = *reinterpret_cast<const uint4*>(o_part + ((size_t)sk * rows + rrow) * D + col);
+      }
+      float mb = ls[0];
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const bool use = ls[k] != -INFINITY;
-          const float wt = use ? expf(ls[k] - m) : 0.f;
-          l += wt;
-          float x[8];
-          unpack8<BF16>(w[k], x);
+      for (int k = 1; k < kBatch; ++k) mb = fmaxf(mb, ls[k]);
+      if (mb > m) {
+        // a group with a larger LSE: rescale what was gathered (nothing yet
+        // while m is -inf)
+        const float sc = m == -INFINITY ? 0.f : expf(m - mb);
+        l *= sc;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = use ? fmaf(wt, x[e], acc[e]) : acc[e];
-        }
+        for (int e = 0; e < 8; ++e) acc[e] *= sc;
+        m = mb;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const bool use = ls[k] != -INFINITY;
+        const float wt = use ? expf(ls[k] - m) : 0.f;
+        l += wt;
+        float x[8];
+        unpack8<BF16>(w[k], x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = use ? fmaf(wt, x[e], acc[e]) : acc[e];
       }
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
