@@ -55,7 +55,13 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const uint16_t* _
   constexpr int kTileWords = D / 4 + 1; // staging row stride (transposed output)
   __shared__ float warp_max[kWarps];
   __shared__ uint32_t tile[TRANSPOSED ? kRowsPerBlock * kTileWords : 1];
+  // the d signs, staged once per CTA so that each lane reads its flip masks
+  // as four-byte words (ordered before their use by the block-max barrier)
+  __shared__ __align__(16) int8_t sgn[ROTATE ? D : 16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if constexpr (ROTATE) {
+    if (threadIdx.x < D) sgn[threadIdx.x] = signs[threadIdx.x];
+  }
   const int q = lane & 3;
   const int bh = blockIdx.x / nblk;
   const int blk = blockIdx.x - bh * nblk;
@@ -82,16 +88,7 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const uint16_t* _
     }
   }
 
-  uint32_t flip[W];  // 0x80 in each byte whose sign is negative
   if constexpr (ROTATE) {
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const int i0 = 32 * (w >> 1) + 8 * q + 4 * (w & 1);
-      uint32_t f = 0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) f |= (signs[i0 + b] < 0 ? 0x80u : 0u) << (8 * b);
-      flip[w] = f;
-    }
     // register butterflies: stride 1 scalar, strides 2..E/2 on packed pairs
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
@@ -148,6 +145,14 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const uint16_t* _
 
   uint32_t code[W];
   const float mult = ROTATE ? __fdiv_rn(inv_sqrt_d, s) : __frcp_rn(s);
+  // 0x80 in each byte whose sign is negative (bit 7 of the int8 sign)
+  uint32_t flip[W];
+  if constexpr (ROTATE) {
+#pragma unroll
+    for (int w = 0; w < W; ++w)
+      flip[w] = *reinterpret_cast<const uint32_t*>(sgn + 32 * (w >> 1) + 8 * q + 4 * (w & 1)) &
+                0x80808080u;
+  }
   const float2 mult2 = f2(mult, mult);
   bool agree = true;
 #pragma unroll
