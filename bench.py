@@ -779,7 +779,7 @@ def cpu_oracle_sample(budget_s: float = 20.0):
 # components on [2,16,8192,128] causal, and the other head dims' forward and
 # backward on [2,16,8192,d] bf16 causal.
 CASES = ("fwd", "bwd", "quant", "fwd_fp8", "fwd_d64", "bwd_d64", "fwd_d96", "bwd_d96",
-         "fwd_d192", "bwd_d192", "fwd_d256", "bwd_d256")
+         "fwd_d192", "bwd_d192", "fwd_d256", "bwd_d256", "merge")
 
 
 def run_case(name, steps, warmup):
@@ -793,6 +793,16 @@ def run_case(name, steps, warmup):
             st.run(c)
         fn = lambda: st.run(name)  # noqa: E731
         w = WORKLOAD
+    elif name == "merge":
+        # the split-KV merge of the step's workload: the partials of a 4-way
+        # split of the keys, computed once, merged on every call
+        w = WORKLOAD
+        g = torch.Generator(device=dev).manual_seed(1234)
+        q, k, v = (torch.randn((w.B, w.H, w.N, w.d), generator=g, device=dev)
+                   .to(torch.bfloat16) for _ in range(3))
+        op, lp = attn.fwd_split(q, k, v, SPLIT_KV_N, causal=w.causal, scale=w.scale)
+        o, lse = attn.merge(op, lp)
+        fn = lambda: attn.merge(op, lp, out=o, lse=lse)  # noqa: E731
     elif name in CASES:
         kind, d = name.split("_d")
         w = WORKLOAD.with_(d=int(d))
