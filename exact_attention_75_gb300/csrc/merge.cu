@@ -18,10 +18,12 @@
 // first; grid-stride over rows; arithmetic in fp32.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
+#include <atomic>
 #include <cstdint>
 
 #include "merge.cuh"
 #include "sm103_ptx.cuh"
+#include "smem_attr.cuh"
 
 namespace attn {
 
@@ -111,20 +113,34 @@ __global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__
   }
 }
 
+// The grid is what the SMs hold at once (the grid-stride loop then gives
+// every CTA the same number of rows, with no partial last wave).  CTAs per
+// SM are queried once per device and instantiation.
+template <int D, bool BF16>
+cudaError_t launch_db(const MergeLaunch& a) {
+  static std::atomic<int> resident[kMaxAttrDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kMaxAttrDevices;
+  int per_sm = tracked ? resident[dev].load(std::memory_order_acquire) : 0;
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_kernel<D, BF16>, 256, 0);
+    if (e != cudaSuccess) return e;
+    if (tracked) resident[dev].store(per_sm, std::memory_order_release);
+  }
+  long blocks = (a.rows + 7) / 8;  // 8 warps (rows) per block
+  const long cap = (long)a.num_sms * (per_sm > 0 ? per_sm : 1);
+  if (blocks > cap) blocks = cap;
+  merge_kernel<D, BF16><<<(int)blocks, 256, 0, a.stream>>>(
+      static_cast<const uint16_t*>(a.o_part), a.lse_part, a.n_split, a.rows,
+      static_cast<uint16_t*>(a.o), a.lse);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_d(const MergeLaunch& a) {
-  long blocks = (a.rows + 7) / 8;  // 8 warps (rows) per block
-  const long cap = (long)a.num_sms * 16;
-  if (blocks > cap) blocks = cap;
-  const auto* op = static_cast<const uint16_t*>(a.o_part);
-  auto* out = static_cast<uint16_t*>(a.o);
-  if (a.bf16)
-    merge_kernel<D, true><<<(int)blocks, 256, 0, a.stream>>>(op, a.lse_part, a.n_split, a.rows,
-                                                             out, a.lse);
-  else
-    merge_kernel<D, false><<<(int)blocks, 256, 0, a.stream>>>(op, a.lse_part, a.n_split,
-                                                              a.rows, out, a.lse);
-  return cudaGetLastError();
+  return a.bf16 ? launch_db<D, true>(a) : launch_db<D, false>(a);
 }
 
 }  // namespace
