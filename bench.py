@@ -50,9 +50,10 @@ LAUNCHES = {"fwd": 1, "bwd": 3, "quant": 3, "fwd_fp8": 1}  # kernels per compone
 
 # Sources whose hash identifies the kernel an ncu traffic figure was taken on.
 KERNEL_SOURCES = {
-    "fwd": ["fwd.cu", "fwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh"],
+    "fwd": ["fwd.cu", "fwd_wide.cu", "fwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh"],
     "fwd_fp8": ["fwd.cu", "fwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh"],
-    "bwd": ["bwd.cu", "bwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh", "unit_ring.cuh"],
+    "bwd": ["bwd.cu", "bwd_wide.cu", "bwd.cuh", "sm103_ptx.cuh", "tiles.cuh", "smem_attr.cuh",
+            "unit_ring.cuh"],
     "quant": ["fp8.cu", "fp8.cuh", "sm103_ptx.cuh"],
 }
 
