@@ -77,6 +77,29 @@ def test_merge_kernel_vs_oracle_merge(attn_lib, d):
     assert not to64(O)[~fin].any()
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_merge_of_the_most_splits(attn_lib, d):
+    """256 partials (the most attn_merge takes; its reads go four splits at a
+    time) with most splits empty for some rows and rows of every kind of
+    spread, against the oracle's merge."""
+    g = torch.Generator().manual_seed(256 + d)
+    S, B, H, N = 256, 1, 2, 45
+    Op = torch.randn((S, B, H, N, d), generator=g).to(torch.bfloat16)
+    Lp = (torch.randn((S, B, H, N), generator=g) * 8.0).to(torch.float32)
+    Lp[torch.rand((S, B, H, N), generator=g) < 0.7] = float("-inf")
+    Lp[:, 0, 1, 3] = float("-inf")      # a row without keys
+    Lp[:, 0, 0, 7] = float("-inf")
+    Lp[200, 0, 0, 7] = 3.0              # a row with one split only, late in the order
+    O, L = attn_lib.merge(Op.cuda(), Lp.cuda())
+    assert attn_lib.poll_status() == (0, 0)
+    O_ref, L_ref = oracle.merge_partials(to64(Op), to64(Lp))
+    assert np.max(np.abs(to64(O) - O_ref)) <= O_TOL
+    fin = np.isfinite(L_ref)
+    assert np.array_equal(fin, np.isfinite(to64(L)))
+    assert np.max(np.abs(to64(L)[fin] - L_ref[fin])) <= 1e-4
+    assert not to64(O)[~fin].any()
+
+
 def test_split_one_equals_fwd(attn_lib):
     w = wl.Workload("t", "fwd", 1, 2, 700, 128, "bf16", True, seed=3)
     (q, k, v), _ = _inputs(w)
