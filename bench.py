@@ -560,7 +560,7 @@ def tensor_peaks(dev, stream, iters=20):
 def decode_timing(attn, dev, stream, peaks, iters=20):
     """Decoding against a key/value cache, timed apart from the step: one
     query per sequence, 16 sequences x 16 heads, an 8192-row bf16 d=128
-    cache, split over the keys into 4 runs (attn_fwd_kv) and merged
+    cache, split over the keys into 8 runs (attn_fwd_kv) and merged
     (attn_merge); and the same with 2 key/value heads.  HBM-bound: the algorithmic bytes are the cache's K and V
     read once (plus q, the partials and O, under 0.1 %).  Inputs are seeded
     standard normals drawn on the device (timing only; parity is in the
@@ -588,6 +588,13 @@ def decode_timing(attn, dev, stream, peaks, iters=20):
             raise RuntimeError(f"device status after the decode timing: {status}")
         r = _summary(ts)
         kv_bytes = 2 * w.B * hkv * w.N * w.d * 2
+        # Context for the fraction: the same bytes read by a plain library
+        # reduction under the same flush (a short read-only kernel also pays
+        # the flush's dirty lines being written back and its own ramp).
+        kv = torch.cat([k.reshape(-1), v.reshape(-1)]).view(torch.int64)
+        r["read_same_bytes_ms"] = round(statistics.median(
+            _timed(lambda: kv.sum(), stream, flush, iters)), 4)
+        del kv
         gbs = kv_bytes / (r["ms_median"] * 1e-3) / 1e9
         r.update({"workload": w.name, "kv_heads": hkv, "n_split": n_split,
                   "queries": wl.DECODE_NQ, "gbs": round(gbs, 1),
@@ -597,9 +604,11 @@ def decode_timing(attn, dev, stream, peaks, iters=20):
                                "algorithmic_bytes": kv_bytes}})
         out["mha" if hkv == w.H else "gqa"] = r
         del q, k, v, Op, Lp, O, L
-    out["note"] = ("fwd_kv (key splits) + merge, L2 flushed, timed apart from the step "
+    out["note"] = ("fwd_kv (key splits, the warp-level decoding kernel: at most 16 query "
+                   "rows per key/value head) + merge, L2 flushed, timed apart from the step "
                    "(not in value); gqa: 16 query heads on 2 key/value heads, a group's "
-                   "8 queries in one tile")
+                   "8 queries in one unit; read_same_bytes_ms: torch.sum over the same K/V "
+                   "bytes under the same flush")
     return out
 
 
@@ -780,7 +789,7 @@ def cpu_oracle_sample(budget_s: float = 20.0):
 # components on [2,16,8192,128] causal, and the other head dims' forward and
 # backward on [2,16,8192,d] bf16 causal.
 CASES = ("fwd", "bwd", "quant", "fwd_fp8", "fwd_d64", "bwd_d64", "fwd_d96", "bwd_d96",
-         "fwd_d192", "bwd_d192", "fwd_d256", "bwd_d256", "merge")
+         "fwd_d192", "bwd_d192", "fwd_d256", "bwd_d256", "merge", "decode", "decode_gqa")
 
 
 def run_case(name, steps, warmup):
@@ -804,6 +813,19 @@ def run_case(name, steps, warmup):
         op, lp = attn.fwd_split(q, k, v, SPLIT_KV_N, causal=w.causal, scale=w.scale)
         o, lse = attn.merge(op, lp)
         fn = lambda: attn.merge(op, lp, out=o, lse=lse)  # noqa: E731
+    elif name in ("decode", "decode_gqa"):
+        # the decode batch's forward over the key splits (16 or 2 key/value
+        # heads), without the merge
+        w = wl.DECODE_BF16_D128
+        hkv = w.H if name == "decode" else wl.DECODE_GQA_KV_HEADS
+        g = torch.Generator(device=dev).manual_seed(1234)
+        q = torch.randn((w.B, w.H, wl.DECODE_NQ, w.d), generator=g, device=dev) \
+            .to(torch.bfloat16)
+        k, v = (torch.randn((w.B, hkv, w.N, w.d), generator=g, device=dev).to(torch.bfloat16)
+                for _ in range(2))
+        op, lp = attn.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal, scale=w.scale)
+        fn = lambda: attn.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=w.causal,  # noqa: E731
+                                 scale=w.scale, out=op, lse=lp)
     elif name in CASES:
         kind, d = name.split("_d")
         w = WORKLOAD.with_(d=int(d))

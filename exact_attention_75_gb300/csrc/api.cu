@@ -12,6 +12,7 @@
 
 #include "attn.h"
 #include "bwd.cuh"
+#include "decode.cuh"
 #include "fp8.cuh"
 #include "fwd.cuh"
 #include "merge.cuh"
@@ -232,10 +233,39 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
   if (st != ATTN_OK) return st;
-  FwdLaunch a;
   const CUtensorMapDataType dt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
+  // At most 16 query rows per key/value head (decoding: one or a few new
+  // tokens of each query head of a group): the warp-level decoding kernel,
+  // which streams every key and value once.
+  if (!wide && !varlen && (int64_t)(H / Hkv) * N <= kDecodeMaxRows) {
+    if (BHkv * n_split > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
+    DecodeLaunch a;
+    if (!encode_3d(&a.tmK, k, dt, 2, d, Nk, BHkv, 64, kDecodeKeys) ||
+        !encode_3d(&a.tmV, v, dt, 2, d, Nk, BHkv, 64, kDecodeKeys))
+      return ATTN_ERR_CUDA;
+    DecodeParams& p = a.params;
+    p.q = q;
+    p.o = o;
+    p.lse = lse;
+    p.status = di->status;
+    p.Hkv = Hkv;
+    p.R = (H / Hkv) * N;
+    p.Nq = N;
+    p.Nk = Nk;
+    p.n_split = n_split;
+    p.n_kblocks = (Nk + 127) / 128;
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.o_split = (size_t)BH * N * d;
+    p.lse_split = (size_t)BH * N;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+    a.num_units = (int)(BHkv * n_split);
+    a.stream = static_cast<cudaStream_t>(stream);
+    return launch_result(launch_decode(a, d, dtype == ATTN_BF16));
+  }
+  FwdLaunch a;
   // tensor-map head index: (batch, head) for dense tensors, head for packed ones
   const int64_t zq = varlen ? H : BH, zkv = varlen ? Hkv : BHkv;
   // Grouped heads whose queries fit one tile together (decoding: few

@@ -124,7 +124,10 @@ attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_
  *   at least Nk - Nq + 1 keys); causal = 0 sees all Nk keys.  Nq = Nk gives
  *   attn_fwd_split (attn_fwd_gqa).  The split covers ceil(Nk/128) key
  *   blocks.  Other arguments and errors as in attn_fwd_split and
- *   attn_fwd_gqa.
+ *   attn_fwd_gqa.  With at most 16 query rows per key/value head
+ *   ((Hq/Hkv) * Nq <= 16, d <= 128) the call runs a decoding kernel that
+ *   reads every key and value once (any dense forward entry point of that
+ *   shape does); the results follow the same definition.
  * Cite: the FlashAttention-2 review, "Discussion Points" (decoding with a
  * KV cache by a kernel that splits the keys, then combines the parts).
  */

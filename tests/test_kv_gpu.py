@@ -51,6 +51,14 @@ def _check(attn, q, k, v, causal, n_split, scale):
     (1, 16, 1, 8, 1000, 64, "fp16", 2),    # 16 x 8 = 128 rows: a full shared tile
     (1, 9, 3, 40, 700, 96, "bf16", 1),     # 3 x 40 = 120 rows
     (1, 8, 2, 20, 20, 128, "bf16", 1),     # Nq = Nk, shared tile, causal top-left
+    # at most 16 rows per key/value head: the warp-level decoding kernel
+    (2, 16, 1, 1, 1000, 128, "bf16", 3),   # 16 heads x 1 query = 16 rows
+    (1, 8, 1, 2, 130, 64, "fp16", 2),      # 8 x 2 = 16 rows, the last key seen by one
+    (1, 6, 2, 4, 333, 96, "fp16", 1),      # 3 x 4 = 12 rows: both halves of the M = 16
+    (1, 5, 1, 3, 77, 128, "bf16", 7),      # 15 rows; 7 splits of one block, 6 empty
+    (1, 2, 2, 5, 5, 64, "bf16", 1),        # Nk = Nq = 5, under one 16-key block
+    (3, 4, 4, 1, 4099, 128, "fp16", 256),  # 33 blocks over 256 splits, most empty
+    (1, 17, 1, 1, 300, 128, "bf16", 2),    # 17 rows: the tiled forward again
 ])
 def test_queries_against_a_cache(attn_lib, causal, B, Hq, Hkv, Nq, Nk, d, dtype, n_split):
     w = wl.Workload("kv", "fwd", B, Hq, Nk, d, dtype, causal, seed=Nq + Nk + d)
@@ -98,6 +106,39 @@ def test_decode_workload_sampled_heads(attn_lib, kv_heads):
         O_ref, L_ref = oracle.attention_kv(q64, k64, v64, w.causal, w.scale, 1)
         assert np.max(np.abs(to64(O[b, h]) - O_ref[0, 0, 0])) <= O_TOL
         assert np.max(np.abs(to64(L[b, h]) - L_ref[0, 0, 0])) <= LSE_TOL
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (96, "fp16"), (128, "bf16")])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,N", [(3, 2), (1, 9), (2, 16)])
+def test_short_sequences_through_the_plain_forward(attn_lib, d, dtype, causal, H, N):
+    """attn_fwd on sequences of at most 16 rows (the decoding kernel: Nk =
+    N, causal top-left), element by element against the oracle."""
+    w = wl.Workload("short", "fwd", 2, H, N, d, dtype, causal, seed=N + d)
+    inp = wl.make_inputs(w)
+    o, lse = attn_lib.fwd(*(inp[n].cuda() for n in ("q", "k", "v")), causal=causal,
+                          scale=w.scale)
+    assert attn_lib.poll_status() == (0, 0)
+    O_ref, L_ref = oracle.attention(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), causal,
+                                    w.scale)
+    assert np.max(np.abs(to64(o) - O_ref)) <= O_TOL
+    assert np.max(np.abs(to64(lse) - L_ref)) <= LSE_TOL
+
+
+@pytest.mark.parametrize("gain", [4.0, 0.01])
+def test_decoding_with_large_and_small_logits(attn_lib, gain):
+    """Queries scaled by `gain` (8 grouped heads, 2 queries each, against
+    3000 keys in 2 splits): large logits make the running maximum rise block
+    after block (the rescale of O in every warp), tiny ones give a nearly
+    uniform softmax; results bitwise the same from run to run."""
+    w = wl.Workload("kv", "fwd", 2, 16, 3000, 128, "bf16", True, seed=21)
+    inp = wl.make_inputs(w)
+    q = (inp["q"][:, :, -2:].float() * gain).to(torch.bfloat16).contiguous()
+    k, v = inp["k"][:, ::8].contiguous(), inp["v"][:, ::8].contiguous()
+    _check(attn_lib, q, k, v, True, 2, w.scale)
+    a = attn_lib.fwd_kv(q.cuda(), k.cuda(), v.cuda(), 2, causal=True, scale=w.scale)
+    b = attn_lib.fwd_kv(q.cuda(), k.cuda(), v.cuda(), 2, causal=True, scale=w.scale)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
 def test_more_queries_than_keys_is_rejected(attn_lib):

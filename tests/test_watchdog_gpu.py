@@ -129,3 +129,27 @@ def test_wide_kernels_wind_down_when_waits_run_out(attn_lib, d):
         assert np.max(np.abs(to64(lse[b, h]) - L_ref)) <= 5e-3
         for g, r in zip((dq, dk, dv), refs):
             assert np.max(np.abs(to64(g[b, h]) - r[b, h])) <= 5e-2 * np.max(np.abs(r[b, h]))
+
+
+def test_decoding_kernel_winds_down_when_waits_run_out(attn_lib):
+    """The same for the decoding kernel (each warp streams its key/value
+    blocks through a ring of its own): one query per head, 16 sequences x 16
+    heads against an 8192-row cache in 4 splits, 1024 CTAs whose first copies
+    queue behind each other's for longer than 1 us.  A launch whose waits run
+    out reports ATTN_ERR_TIMEOUT; the next launch at the normal limit matches
+    the oracle on the first and the last head."""
+    import numpy as np
+    import oracle
+    from helpers import to64
+    w = wl.DECODE_BF16_D128
+    inp = wl.make_decode_inputs(w, kv_heads=w.H)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    attn_lib.poll_status()
+    _expect_timeout(attn_lib, lambda: attn_lib.fwd_kv(q, k, v, 4, causal=w.causal, scale=w.scale))
+    Op, Lp = attn_lib.fwd_kv(q, k, v, 4, causal=w.causal, scale=w.scale)
+    assert attn_lib.poll_status() == (0, 0)
+    for b, h in [(0, 0), (w.B - 1, w.H - 1)]:
+        O_ref, L_ref = oracle.attention_kv(*(to64(inp[n][b:b + 1, h:h + 1]) for n in ("q", "k", "v")),
+                                           w.causal, w.scale, 4)
+        assert np.max(np.abs(to64(Op[:, b, h]) - O_ref[:, 0, 0])) <= 2e-2
+        assert np.max(np.abs(to64(Lp[:, b, h]) - L_ref[:, 0, 0])) <= 5e-3

@@ -90,7 +90,9 @@ WORKLOADS = [TINY_FWD_FP16, FWD_FP16_D64, FWD_BF16_D128, BWD_BF16_D128, FWD_FP8_
 DECODE_BF16_D128 = Workload("decode_bf16_b16h16nk8192d128", "fwd_kv", 16, 16, 8192, 128, "bf16",
                             True)
 DECODE_NQ = 1
-DECODE_SPLITS = 4
+# Key splits of the decode batches: 8 (256 CTAs with grouped heads, 2048 for
+# the multi-head batch) timed fastest of 1 ... 32 for both.
+DECODE_SPLITS = 8
 # The same batch with grouped heads: 16 query heads sharing 2 key/value heads
 # (a group's 8 queries share one query tile).
 DECODE_GQA_KV_HEADS = 2
