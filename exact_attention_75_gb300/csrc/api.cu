@@ -226,20 +226,22 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   if (Nk == 0) Nk = N;
   if (Nk < N || (varlen && Nk != N) || !shape_ok(B, Hkv, Nk, d)) return ATTN_ERR_INVALID_ARG;
-  // The wide head dims run one query tile per unit, dense or grouped heads
-  // only: no key split, key cache or packed variable-length batch.
+  // At most 16 query rows per key/value head (decoding: one or a few new
+  // tokens of each query head of a group) run on the warp-level decoding
+  // kernel, which streams every key and value once, at every head dim.
+  const bool decode = !varlen && (int64_t)(H / Hkv) * N <= kDecodeMaxRows;
+  // Otherwise the wide head dims run one query tile per unit, dense or
+  // grouped heads only: no key split, key cache or packed variable-length
+  // batch.
   const bool wide = d > 128;
-  if (wide && (n_split != 1 || varlen || Nk != N)) return ATTN_ERR_UNSUPPORTED;
+  if (wide && !decode && (n_split != 1 || varlen || Nk != N)) return ATTN_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
   if (st != ATTN_OK) return st;
   const CUtensorMapDataType dt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
-  // At most 16 query rows per key/value head (decoding: one or a few new
-  // tokens of each query head of a group): the warp-level decoding kernel,
-  // which streams every key and value once.
-  if (!wide && !varlen && (int64_t)(H / Hkv) * N <= kDecodeMaxRows) {
+  if (decode) {
     if (BHkv * n_split > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
     DecodeLaunch a;
     if (!encode_3d(&a.tmK, k, dt, 2, d, Nk, BHkv, 64, kDecodeKeys) ||
@@ -374,7 +376,7 @@ attn_status attn_merge(const void* o_part, const float* lse_part, int n_split, v
   if (n_split < 1 || n_split > 256) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
   if (!shape_ok(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);

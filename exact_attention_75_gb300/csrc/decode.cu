@@ -7,15 +7,16 @@
 // those HBM reads; the tiled forward would spend a whole 128-row softmax per
 // key block on these few rows.
 //
-// One CTA of four warps per (batch, key/value head, split).  The split's
-// keys are cut into blocks of 16 and the warps take them in turn (warp w:
-// blocks w, w + 4, ...).  Each warp streams its own blocks through a private
+// d in {64, 96, 128, 192, 256}.  One CTA of four warps per (batch,
+// key/value head, split).  The split's keys are cut into blocks of 16 and
+// the warps take them in turn (warp w: blocks w, w + 4, ...).  Each warp streams its own blocks through a private
 // ring of shared-memory slots: its lane 0 issues the TMA copies (K and V of a
 // block, 64-column boxes with the 128-byte swizzle) and refills a slot as soon
 // as the warp has multiplied it, so no warp ever waits for another before the
 // end.  Per block, on the warp-level tensor-core product (m16n8k16, fp32
 // accumulation; the 16 rows of its M hold the unit's R query rows):
-//   S = Q K^T        A = Q (fragments kept in registers), B = K by ldmatrix;
+//   S = Q K^T        A = Q (fragments in registers up to d = 128, above by
+//                    ldmatrix from a copy in shared memory), B = K by ldmatrix;
 //   online softmax   per row the block maximum raises the warp's running
 //                    maximum m, P = exp2(S scale log2 e - m), the running sum
 //                    and O scaled by exp2(m_old - m_new) (FlashAttention-2
@@ -46,16 +47,22 @@ template <int D>
 struct DecodeLayout {
   static constexpr int kChunks = (D + 63) / 64;               // 64-column chunks of a row
   static constexpr int kSlotBytes = 2 * kChunks * kBoxBytes;  // K chunks, then V chunks
-  static constexpr int kSlots = D == 64 ? 6 : 3;              // ring depth of each warp
+  // Ring depth of each warp: two CTAs per SM up to d = 192, one at d = 256.
+  static constexpr int kSlots = D == 64 ? 6 : (D == 192 ? 2 : 3);
   static constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;
+  // Above d = 128 the Q fragments are read from shared memory (16 rows in
+  // the layout of a staged block) rather than held in registers.
+  static constexpr bool kQSmem = D > 128;
+  static constexpr int kQBytes = kQSmem ? kChunks * kBoxBytes : 0;
   // After the loop the ring holds each warp's O (16 rows, padded), m and l.
   static constexpr int kRowStride = D + 4;
   static constexpr int kRedBytes = kWarps * 16 * (kRowStride + 2) * 4;
-  static constexpr int kDataBytes = kRingBytes > kRedBytes ? kRingBytes : kRedBytes;
-  static constexpr int kBarOff = kDataBytes;  // one mbarrier per slot
+  static_assert(kRingBytes >= kRedBytes && kRingBytes % 1024 == 0, "ring layout");
+  static constexpr int kQOff = kRingBytes;
+  static constexpr int kBarOff = kQOff + kQBytes;  // one mbarrier per slot
   static constexpr int kFlagOff = kBarOff + kWarps * kSlots * 8;
   static constexpr int kBytes = kFlagOff + 16 + 1024;  // + room to align the base
-  static_assert(kBytes <= 113 * 1024, "two CTAs per SM");
+  static_assert(kBytes <= (D == 256 ? 227 : 113) * 1024, "CTAs per SM");
 };
 
 // Byte offset of 16-byte piece `piece` (8 columns) of row `row` in a staged
@@ -156,19 +163,35 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
   // Q fragments of the 16 rows (rows >= R are zero), A layout of m16n8k16:
   // a0 (row r0, cols c..c+1), a1 (row r0 + 8), a2 (row r0, cols c+8..),
-  // a3 (row r0 + 8, cols c+8..), c = 16 ks + 2 (lane % 4).
+  // a3 (row r0 + 8, cols c+8..), c = 16 ks + 2 (lane % 4).  Up to d = 128
+  // they stay in registers; above, Q is staged once in shared memory and
+  // each k-step's fragment read by ldmatrix (matrix i: rows 8 (i % 2)..,
+  // columns 16 ks + 8 (i / 2)..).
   const int r0 = lane >> 2, cq = 2 * (lane & 3);
   const uint16_t* qu = static_cast<const uint16_t*>(p.q) + (size_t)bk * p.R * D;
-  auto qword = [&](int r, int c) -> uint32_t {
-    return r < p.R ? *reinterpret_cast<const uint32_t*>(qu + (size_t)r * D + c) : 0u;
-  };
-  uint32_t qa[KS][4];
+  constexpr int KSR = L::kQSmem ? 1 : KS;  // k-steps held in registers
+  uint32_t qa[KSR][4];
+  const uint32_t qs = sbase + L::kQOff;
+  const int qrow = (lane & 7) + 8 * ((lane >> 3) & 1);
+  if constexpr (L::kQSmem) {
+    for (int i = threadIdx.x; i < 16 * (D / 8); i += kThreads) {
+      const int r = i / (D / 8), pc = i % (D / 8);
+      const uint4 x = r < p.R ? *reinterpret_cast<const uint4*>(qu + (size_t)r * D + 8 * pc)
+                              : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + L::kQOff + sw_off(r, pc)) = x;
+    }
+    __syncthreads();
+  } else {
+    auto qword = [&](int r, int c) -> uint32_t {
+      return r < p.R ? *reinterpret_cast<const uint32_t*>(qu + (size_t)r * D + c) : 0u;
+    };
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    qa[ks][0] = qword(r0, 16 * ks + cq);
-    qa[ks][1] = qword(r0 + 8, 16 * ks + cq);
-    qa[ks][2] = qword(r0, 16 * ks + cq + 8);
-    qa[ks][3] = qword(r0 + 8, 16 * ks + cq + 8);
+    for (int ks = 0; ks < KSR; ++ks) {
+      qa[ks][0] = qword(r0, 16 * ks + cq);
+      qa[ks][1] = qword(r0 + 8, 16 * ks + cq);
+      qa[ks][2] = qword(r0, 16 * ks + cq + 8);
+      qa[ks][3] = qword(r0 + 8, 16 * ks + cq + 8);
+    }
   }
   // Last key each of the thread's two rows sees (-1: a padding row, no key).
   auto last_key = [&](int r) {
@@ -196,17 +219,30 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const uint32_t tv = tk + L::kChunks * kBoxBytes;
     const int key0 = k_lo + (warp + j * kWarps) * kDecodeKeys;
 
-    // S = Q K^T: ldmatrix of one 8-key tile over two k-steps (pieces 2ks..2ks+3).
+    // S = Q K^T, two k-steps at a time: ldmatrix of one 8-key tile over
+    // pieces 2ks..2ks+3, the two key tiles' products interleaved.
     float sc[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < KS; ks += 2) {
+    for (int ks = 0; ks < KS; ks += 2) {
+      uint32_t qx[4], qy[4];
+      if constexpr (L::kQSmem) {
+        ldsm_x4(qs + sw_off(qrow, 2 * ks + (lane >> 4)), qx);
+        ldsm_x4(qs + sw_off(qrow, 2 * ks + 2 + (lane >> 4)), qy);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qx[e] = qa[ks][e];
+          qy[e] = qa[ks + 1][e];
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
         uint32_t b[4];
         ldsm_x4(tk + sw_off(8 * nt + (lane & 7), 2 * ks + (lane >> 3)), b);
-        mma16816<BF16>(sc[nt], qa[ks], b[0], b[1]);
-        mma16816<BF16>(sc[nt], qa[ks + 1], b[2], b[3]);
+        mma16816<BF16>(sc[nt], qx, b[0], b[1]);
+        mma16816<BF16>(sc[nt], qy, b[2], b[3]);
       }
     }
 
@@ -383,9 +419,13 @@ cudaError_t launch_d(const DecodeLaunch& a, bool bf16) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeLaunch& a, int d, bool bf16) {
-  if (d == 64) return launch_d<64>(a, bf16);
-  if (d == 96) return launch_d<96>(a, bf16);
-  return launch_d<128>(a, bf16);
+  switch (d) {
+    case 64: return launch_d<64>(a, bf16);
+    case 96: return launch_d<96>(a, bf16);
+    case 192: return launch_d<192>(a, bf16);
+    case 256: return launch_d<256>(a, bf16);
+    default: return launch_d<128>(a, bf16);
+  }
 }
 
 }  // namespace attn

@@ -11,7 +11,7 @@
 //
 // d/8 lanes per row (8 values, one 16-byte read of each split's row per
 // lane), so a warp merges 32/(d/8) rows at once (rounded down: at d = 96
-// lanes 24-31 idle).  One pass over the splits, four at a time (their LSE
+// lanes 24-31 idle; at d = 192 and 256 one row per warp).  One pass over the splits, four at a time (their LSE
 // and O reads in flight together): the running maximum m rises with each
 // group and the sums gathered so far are scaled by exp(m_old - m_new), as in
 // the online softmax, so no separate pass over the LSEs waits on memory
@@ -146,8 +146,13 @@ cudaError_t launch_d(const MergeLaunch& a) {
 }  // namespace
 
 cudaError_t launch_merge(const MergeLaunch& a) {
-  if (a.d == 96) return launch_d<96>(a);
-  return a.d == 128 ? launch_d<128>(a) : launch_d<64>(a);
+  switch (a.d) {
+    case 64: return launch_d<64>(a);
+    case 96: return launch_d<96>(a);
+    case 192: return launch_d<192>(a);
+    case 256: return launch_d<256>(a);
+    default: return launch_d<128>(a);
+  }
 }
 
 }  // namespace attn

@@ -21,9 +21,11 @@
  *    contiguous (d innermost); LSE and the delta vector D are [B, H, N].
  *    All pointers are DEVICE pointers, 16-byte aligned (TMA requirement).
  *  - Shapes: d in {64, 96, 128}; attn_fwd, attn_fwd_gqa, attn_bwd,
- *    attn_bwd_gqa and attn_bwd_noalloc also take d in {192, 256} (the key
- *    split, key cache and variable-length entry points return
- *    ATTN_ERR_UNSUPPORTED there; the FP8 entry points: as stated there);
+ *    attn_bwd_gqa, attn_bwd_noalloc and attn_merge also take d in
+ *    {192, 256}, and so do attn_fwd_split and attn_fwd_kv with at most 16
+ *    query rows per key/value head (otherwise the key split, key cache and
+ *    variable-length entry points return ATTN_ERR_UNSUPPORTED there; the
+ *    FP8 entry points: as stated there);
  *    N >= 1 (any N: partial tiles are zero-filled on load and masked);
  *    B, H >= 1; B*H*N*d must fit in 2^31 elements.
  *  - Causal masking is top-left aligned: key j is visible to query i iff
@@ -125,9 +127,10 @@ attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_
  *   attn_fwd_split (attn_fwd_gqa).  The split covers ceil(Nk/128) key
  *   blocks.  Other arguments and errors as in attn_fwd_split and
  *   attn_fwd_gqa.  With at most 16 query rows per key/value head
- *   ((Hq/Hkv) * Nq <= 16, d <= 128) the call runs a decoding kernel that
- *   reads every key and value once (any dense forward entry point of that
- *   shape does); the results follow the same definition.
+ *   ((Hq/Hkv) * Nq <= 16) the call runs a decoding kernel that reads every
+ *   key and value once (any dense forward entry point of that shape does),
+ *   at d in {64, 96, 128, 192, 256}; with more rows d must be <= 128.  The
+ *   results follow the same definition.
  * Cite: the FlashAttention-2 review, "Discussion Points" (decoding with a
  * KV cache by a kernel that splits the keys, then combines the parts).
  */
@@ -143,7 +146,7 @@ attn_status attn_fwd_kv(const void* q, const void* k, const void* v, void* o_par
  *   o_part   : [n_split, B, H, N, d] fp16/bf16 (dtype), read only.
  *   lse_part : [n_split, B, H, N] fp32, read only.
  *   o        : [B, H, N, d] dtype, written;  lse : [B, H, N] fp32, written.
- * d in {64, 96, 128}; 1 <= n_split <= 256.
+ * d in {64, 96, 128, 192, 256}; 1 <= n_split <= 256.
  * Cite: the FlashAttention-2 review, "Insights" (the log-sum-exp is all that
  * has to be kept besides O); the combine formula follows from the softmax
  * definition over the union of the key sets.

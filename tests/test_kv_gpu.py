@@ -59,6 +59,11 @@ def _check(attn, q, k, v, causal, n_split, scale):
     (1, 2, 2, 5, 5, 64, "bf16", 1),        # Nk = Nq = 5, under one 16-key block
     (3, 4, 4, 1, 4099, 128, "fp16", 256),  # 33 blocks over 256 splits, most empty
     (1, 17, 1, 1, 300, 128, "bf16", 2),    # 17 rows: the tiled forward again
+    # the wide head dims: only the decoding kernel's shapes
+    (2, 8, 1, 1, 1000, 256, "bf16", 3),    # 8 rows, Q fragments from shared memory
+    (1, 4, 2, 6, 555, 256, "fp16", 2),     # 12 rows, both halves of M
+    (1, 16, 2, 2, 700, 192, "bf16", 5),    # 16 rows
+    (2, 3, 3, 1, 130, 192, "fp16", 1),     # one row per key/value head
 ])
 def test_queries_against_a_cache(attn_lib, causal, B, Hq, Hkv, Nq, Nk, d, dtype, n_split):
     w = wl.Workload("kv", "fwd", B, Hq, Nk, d, dtype, causal, seed=Nq + Nk + d)
@@ -108,7 +113,8 @@ def test_decode_workload_sampled_heads(attn_lib, kv_heads):
         assert np.max(np.abs(to64(L[b, h]) - L_ref[0, 0, 0])) <= LSE_TOL
 
 
-@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (96, "fp16"), (128, "bf16")])
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (96, "fp16"), (128, "bf16"), (192, "fp16"),
+                                     (256, "bf16")])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("H,N", [(3, 2), (1, 9), (2, 16)])
 def test_short_sequences_through_the_plain_forward(attn_lib, d, dtype, causal, H, N):
@@ -139,6 +145,29 @@ def test_decoding_with_large_and_small_logits(attn_lib, gain):
     a = attn_lib.fwd_kv(q.cuda(), k.cuda(), v.cuda(), 2, causal=True, scale=w.scale)
     b = attn_lib.fwd_kv(q.cuda(), k.cuda(), v.cuda(), 2, causal=True, scale=w.scale)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_decode_at_the_wide_head_dims(attn_lib, d):
+    """One query per sequence, 8 sequences x 16 query heads on 2 key/value
+    heads against a 4096-row bf16 cache at d = 192 / 256, 8 splits + merge
+    (the decode batch's shape at the wide head dims): four (sequence, head)
+    pairs, the first and the last among them, against the oracle."""
+    w = wl.Workload("kvw", "fwd", 8, 16, 4096, d, "bf16", True, seed=d)
+    inp = wl.make_decode_inputs(w, kv_heads=2)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    Op, Lp = attn_lib.fwd_kv(q, k, v, 8, causal=True, scale=w.scale)
+    O, L = attn_lib.merge(Op, Lp)
+    assert attn_lib.poll_status() == (0, 0)
+    for b, h in [(0, 0), (2, 9), (5, 6), (7, 15)]:
+        q64 = to64(inp["q"][b:b + 1, h:h + 1])
+        k64, v64 = (to64(inp[n][b:b + 1, h // 8:h // 8 + 1]) for n in ("k", "v"))
+        O_ref_p, L_ref_p = oracle.attention_kv(q64, k64, v64, True, w.scale, 8)
+        assert np.max(np.abs(to64(Op[:, b, h]) - O_ref_p[:, 0, 0])) <= O_TOL
+        assert np.max(np.abs(to64(Lp[:, b, h]) - L_ref_p[:, 0, 0])) <= LSE_TOL
+        O_ref, L_ref = oracle.attention_kv(q64, k64, v64, True, w.scale, 1)
+        assert np.max(np.abs(to64(O[b, h]) - O_ref[0, 0, 0])) <= O_TOL
+        assert np.max(np.abs(to64(L[b, h]) - L_ref[0, 0, 0])) <= LSE_TOL
 
 
 def test_more_queries_than_keys_is_rejected(attn_lib):

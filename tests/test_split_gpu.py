@@ -56,7 +56,7 @@ def test_split_partials_and_merge_small(attn_lib, dtype, d, causal, B, H, N, n_s
     assert np.max(np.abs(to64(L) - L_ref)) <= LSE_TOL
 
 
-@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("d", [64, 96, 128, 192, 256])
 def test_merge_kernel_vs_oracle_merge(attn_lib, d):
     """The merge alone on synthetic partials: random O_s, LSE_s of spread
     magnitudes, some -inf (a split without keys) and one all -inf row."""

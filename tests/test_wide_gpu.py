@@ -114,8 +114,9 @@ def test_wide_forward_deterministic(attn_lib):
 
 def test_wide_modes_not_built_are_rejected(attn_lib):
     """The key split, the key cache and packed variable-length batches are
-    built for d <= 128 only: at d = 256 they return ATTN_ERR_UNSUPPORTED
-    before any launch."""
+    built for d <= 128 only, except on the decoding kernel's shapes (at most
+    16 query rows per key/value head): at d = 256 with 64 or 32 rows per head
+    they return ATTN_ERR_UNSUPPORTED before any launch."""
     L = attn_lib.lib()
     x = torch.zeros((1, 1, 64, 256), dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros((2, 1, 1, 64), dtype=torch.float32, device="cuda")
