@@ -789,7 +789,8 @@ def cpu_oracle_sample(budget_s: float = 20.0):
 # components on [2,16,8192,128] causal, and the other head dims' forward and
 # backward on [2,16,8192,d] bf16 causal.
 CASES = ("fwd", "bwd", "quant", "fwd_fp8", "fwd_d64", "bwd_d64", "fwd_d96", "bwd_d96",
-         "fwd_d192", "bwd_d192", "fwd_d256", "bwd_d256", "merge", "decode", "decode_gqa")
+         "fwd_d192", "bwd_d192", "fwd_d256", "bwd_d256", "merge", "decode", "decode_gqa",
+         "fwd_fp16_d64_n512")
 
 
 def run_case(name, steps, warmup):
@@ -813,6 +814,13 @@ def run_case(name, steps, warmup):
         op, lp = attn.fwd_split(q, k, v, SPLIT_KV_N, causal=w.causal, scale=w.scale)
         o, lse = attn.merge(op, lp)
         fn = lambda: attn.merge(op, lp, out=o, lse=lse)  # noqa: E731
+    elif name == "fwd_fp16_d64_n512":
+        # the shortest point of the fp16 d = 64 sweep: [32,16,512,64] causal
+        w = wl.sweep_d64(True)[0]
+        inp = wl.make_inputs(w)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        o, lse = attn.fwd(q, k, v, causal=w.causal, scale=w.scale)
+        fn = lambda: attn.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)  # noqa
     elif name in ("decode", "decode_gqa"):
         # the decode batch's forward over the key splits (16 or 2 key/value
         # heads), without the merge
