@@ -9,6 +9,9 @@ ragged sizes together, and runs one of three paths:
   split  : forward over n_split key ranges (partials against the oracle's
            partials) and the merge of the device partials against the
            oracle's full attention.
+A second set of cases draws decoding shapes (at most 16 query rows per
+key/value head, every head dim including 192 and 256, a ragged cache, 1-12
+key splits) for the key-cache forward and the merge.
 Tolerances as everywhere: |O - O_ref| <= 2e-2, |LSE - LSE_ref| <= 5e-3,
 gradients <= 5e-2 * max |ref| per tensor (an all-zero reference, e.g. N = 1,
 bounds |g| <= 1e-3).
@@ -122,3 +125,47 @@ def _split(attn, c):
 def test_random_feature_combination(attn_lib, seed):
     c = _draw(seed)
     {"dense": _dense, "varlen": _varlen, "split": _split}[c["mode"]](attn_lib, c)
+
+
+DECODE_CASES = 24
+
+
+def _draw_decode(seed):
+    rng = np.random.default_rng(9000 + seed)
+    G = int(rng.integers(1, 9))
+    Nq = int(rng.integers(1, 16 // G + 1))  # G * Nq <= 16 rows per key/value head
+    return {"d": int(rng.choice([64, 96, 128, 192, 256])),
+            "dtype": str(rng.choice(["fp16", "bf16"])),
+            "causal": bool(rng.integers(2)),
+            "B": int(rng.integers(1, 3)),
+            "Hkv": int(rng.integers(1, 3)),
+            "G": G, "Nq": Nq,
+            "Nk": int(rng.integers(Nq, 3000)),
+            "n_split": int(rng.integers(1, 13)),
+            "seed": seed}
+
+
+@pytest.mark.parametrize("seed", range(DECODE_CASES))
+def test_random_decoding_case(attn_lib, seed):
+    c = _draw_decode(seed)
+    Hq = c["Hkv"] * c["G"]
+    w = wl.Workload("fuzzdec", "fwd", c["B"], Hq, c["Nk"], c["d"], c["dtype"], c["causal"],
+                    seed=c["seed"])
+    inp = wl.make_inputs(w)
+    # the queries are the last Nq positions; key/value heads the first head of each group
+    q = inp["q"][:, :, c["Nk"] - c["Nq"]:].contiguous()
+    k, v = inp["k"][:, ::c["G"]].contiguous(), inp["v"][:, ::c["G"]].contiguous()
+    Op, Lp = attn_lib.fwd_kv(q.cuda(), k.cuda(), v.cuda(), c["n_split"], causal=w.causal,
+                             scale=w.scale)
+    O, L = attn_lib.merge(Op, Lp)
+    assert attn_lib.poll_status() == (0, 0), c
+    q64, k64, v64 = to64(q), to64(k), to64(v)
+    O_ref_p, L_ref_p = oracle.attention_kv(q64, k64, v64, w.causal, w.scale, c["n_split"])
+    Lp64 = to64(Lp)
+    assert np.array_equal(np.isneginf(Lp64), np.isneginf(L_ref_p)), c
+    seen = ~np.isneginf(L_ref_p)
+    assert np.max(np.abs(Lp64[seen] - L_ref_p[seen]), initial=0.0) <= LSE_TOL, c
+    assert np.max(np.abs(to64(Op) - O_ref_p)) <= O_TOL, c
+    O_ref, L_ref = oracle.attention_kv(q64, k64, v64, w.causal, w.scale, 1)
+    assert np.max(np.abs(to64(O) - O_ref[0])) <= O_TOL, c
+    assert np.max(np.abs(to64(L) - L_ref[0])) <= LSE_TOL, c
