@@ -228,12 +228,17 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   if (Nk < N || (varlen && Nk != N) || !shape_ok(B, Hkv, Nk, d)) return ATTN_ERR_INVALID_ARG;
   // At most 16 query rows per key/value head (decoding: one or a few new
   // tokens of each query head of a group) run on the warp-level decoding
-  // kernel, which streams every key and value once, at every head dim.
-  const bool decode = !varlen && (int64_t)(H / Hkv) * N <= kDecodeMaxRows;
+  // kernel, which streams every key and value once, at every head dim.  At
+  // the wide head dims, whose tiled kernel has no key split or key cache,
+  // it also takes those modes up to 128 rows per key/value head (16 rows per
+  // unit, the units of a head sharing its key/value reads through L2).
+  const bool wide = d > 128;
+  const int64_t rows_kv = (int64_t)(H / Hkv) * N;
+  const bool decode = !varlen && (rows_kv <= kDecodeMaxRows ||
+                                  (wide && (n_split != 1 || Nk != N) && rows_kv <= kDecodeRowLimit));
   // Otherwise the wide head dims run one query tile per unit, dense or
   // grouped heads only: no key split, key cache or packed variable-length
   // batch.
-  const bool wide = d > 128;
   if (wide && !decode && (n_split != 1 || varlen || Nk != N)) return ATTN_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   attn_status st = device_info(&di);
@@ -242,7 +247,8 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int64_t BH = (int64_t)B * H, BHkv = (int64_t)B * Hkv;
   if (decode) {
-    if (BHkv * n_split > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
+    const int n_rgroups = (int)((rows_kv + kDecodeMaxRows - 1) / kDecodeMaxRows);
+    if (BHkv * n_split * n_rgroups > 0x7FFFFFFF) return ATTN_ERR_INVALID_ARG;
     DecodeLaunch a;
     if (!encode_3d(&a.tmK, k, dt, 2, d, Nk, BHkv, 64, kDecodeKeys) ||
         !encode_3d(&a.tmV, v, dt, 2, d, Nk, BHkv, 64, kDecodeKeys))
@@ -253,7 +259,8 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
     p.lse = lse;
     p.status = di->status;
     p.Hkv = Hkv;
-    p.R = (H / Hkv) * N;
+    p.R = (int)rows_kv;
+    p.n_rgroups = n_rgroups;
     p.Nq = N;
     p.Nk = Nk;
     p.n_split = n_split;
@@ -263,7 +270,7 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
     p.o_split = (size_t)BH * N * d;
     p.lse_split = (size_t)BH * N;
     p.wait_limit_ns = g_wait_limit_ns.load();
-    a.num_units = (int)(BHkv * n_split);
+    a.num_units = (int)(BHkv * n_split * n_rgroups);
     a.stream = static_cast<cudaStream_t>(stream);
     return launch_result(launch_decode(a, d, dtype == ATTN_BF16));
   }

@@ -1,6 +1,6 @@
 // Decoding: a few query rows per key/value head (G grouped query heads x Nq
-// new tokens, R = G Nq <= 16 rows) against a key/value cache, split over the
-// keys like the tiled forward ("8.3 FlashAttention-3" section 7.3 on
+// new tokens, R = G Nq rows, taken 16 at a time) against a key/value cache,
+// split over the keys like the tiled forward ("8.3 FlashAttention-3" section 7.3 on
 // attention over parts of the keys; the FlashAttention-2 review, "Discussion
 // Points", on a decoding kernel that splits the keys and combines the parts).
 // Every key and value of the cache is read once, so the kernel is bound by
@@ -8,7 +8,7 @@
 // key block on these few rows.
 //
 // d in {64, 96, 128, 192, 256}.  One CTA of four warps per (batch,
-// key/value head, split).  The split's keys are cut into blocks of 16 and
+// key/value head, split, group of 16 of the head's R rows).  The split's keys are cut into blocks of 16 and
 // the warps take them in turn (warp w: blocks w, w + 4, ...).  Each warp streams its own blocks through a private
 // ring of shared-memory slots: its lane 0 issues the TMA copies (K and V of a
 // block, 64-column boxes with the 128-byte swizzle) and refills a slot as soon
@@ -128,8 +128,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int s) { return sbase + L::kBarOff + 8u * (uint32_t)(warp * NS + s); };
 
-  const int split = blockIdx.x % p.n_split;
-  const int bk = blockIdx.x / p.n_split;  // batch * Hkv + key/value head
+  // Unit = (key/value head, split, group of 16 rows); the row groups of one
+  // (head, split) are neighbours, so their K/V reads meet in L2.
+  const int rg = blockIdx.x % p.n_rgroups;
+  const int split = (blockIdx.x / p.n_rgroups) % p.n_split;
+  const int bk = blockIdx.x / p.n_rgroups / p.n_split;  // batch * Hkv + key/value head
+  const int row0 = rg * kDecodeMaxRows;                 // first row of the group in the head's R
+  const int rows = min(kDecodeMaxRows, p.R - row0);     // rows of this unit
   const int k_lo = (int)((long long)split * p.n_kblocks / p.n_split) * 128;
   const int k_hi = min((int)((long long)(split + 1) * p.n_kblocks / p.n_split) * 128, p.Nk);
   const int nb = k_hi > k_lo ? (k_hi - k_lo + kDecodeKeys - 1) / kDecodeKeys : 0;
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   // each k-step's fragment read by ldmatrix (matrix i: rows 8 (i % 2)..,
   // columns 16 ks + 8 (i / 2)..).
   const int r0 = lane >> 2, cq = 2 * (lane & 3);
-  const uint16_t* qu = static_cast<const uint16_t*>(p.q) + (size_t)bk * p.R * D;
+  const uint16_t* qu = static_cast<const uint16_t*>(p.q) + ((size_t)bk * p.R + row0) * D;
   constexpr int KSR = L::kQSmem ? 1 : KS;  // k-steps held in registers
   uint32_t qa[KSR][4];
   const uint32_t qs = sbase + L::kQOff;
@@ -176,14 +181,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   if constexpr (L::kQSmem) {
     for (int i = threadIdx.x; i < 16 * (D / 8); i += kThreads) {
       const int r = i / (D / 8), pc = i % (D / 8);
-      const uint4 x = r < p.R ? *reinterpret_cast<const uint4*>(qu + (size_t)r * D + 8 * pc)
+      const uint4 x = r < rows ? *reinterpret_cast<const uint4*>(qu + (size_t)r * D + 8 * pc)
                               : make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(smem + L::kQOff + sw_off(r, pc)) = x;
     }
     __syncthreads();
   } else {
     auto qword = [&](int r, int c) -> uint32_t {
-      return r < p.R ? *reinterpret_cast<const uint32_t*>(qu + (size_t)r * D + c) : 0u;
+      return r < rows ? *reinterpret_cast<const uint32_t*>(qu + (size_t)r * D + c) : 0u;
     };
 #pragma unroll
     for (int ks = 0; ks < KSR; ++ks) {
@@ -195,12 +200,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   }
   // Last key each of the thread's two rows sees (-1: a padding row, no key).
   auto last_key = [&](int r) {
-    if (r >= p.R) return -1;
-    const int lim = p.causal ? r % p.Nq + p.Nk - p.Nq : p.Nk - 1;
+    if (r >= rows) return -1;
+    const int lim = p.causal ? (row0 + r) % p.Nq + p.Nk - p.Nq : p.Nk - 1;
     return min(lim, k_hi - 1);
   };
   const int limA = last_key(r0), limB = last_key(r0 + 8);
-  const bool hiB = p.R > 8;  // rows 8..15 hold queries
+  const bool hiB = rows > 8;  // rows 8..15 hold queries
 
   float o[DN][4];
 #pragma unroll
@@ -367,10 +372,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   __syncthreads();
   if (*abort_flag != 0) return;
 
-  uint16_t* ou = static_cast<uint16_t*>(p.o) + (size_t)split * p.o_split + (size_t)bk * p.R * D;
-  float* lu = p.lse + (size_t)split * p.lse_split + (size_t)bk * p.R;
+  uint16_t* ou = static_cast<uint16_t*>(p.o) + (size_t)split * p.o_split +
+                 ((size_t)bk * p.R + row0) * D;
+  float* lu = p.lse + (size_t)split * p.lse_split + (size_t)bk * p.R + row0;
   constexpr int P8 = D / 8;
-  for (int idx = threadIdx.x; idx < p.R * P8; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < rows * P8; idx += kThreads) {
     const int r = idx / P8, c = (idx % P8) * 8;
     float M = -INFINITY;
 #pragma unroll

@@ -22,7 +22,7 @@
  *    All pointers are DEVICE pointers, 16-byte aligned (TMA requirement).
  *  - Shapes: d in {64, 96, 128}; attn_fwd, attn_fwd_gqa, attn_bwd,
  *    attn_bwd_gqa, attn_bwd_noalloc and attn_merge also take d in
- *    {192, 256}, and so do attn_fwd_split and attn_fwd_kv with at most 16
+ *    {192, 256}, and so do attn_fwd_split and attn_fwd_kv with at most 128
  *    query rows per key/value head (otherwise the key split, key cache and
  *    variable-length entry points return ATTN_ERR_UNSUPPORTED there; the
  *    FP8 entry points: as stated there);
@@ -129,8 +129,10 @@ attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o_
  *   attn_fwd_gqa.  With at most 16 query rows per key/value head
  *   ((Hq/Hkv) * Nq <= 16) the call runs a decoding kernel that reads every
  *   key and value once (any dense forward entry point of that shape does),
- *   at d in {64, 96, 128, 192, 256}; with more rows d must be <= 128.  The
- *   results follow the same definition.
+ *   at d in {64, 96, 128, 192, 256}.  At d in {192, 256} the same kernel
+ *   takes up to 128 rows per key/value head, 16 rows per work unit (each
+ *   unit streams the head's keys and values); more rows there return
+ *   ATTN_ERR_UNSUPPORTED.  The results follow the same definition.
  * Cite: the FlashAttention-2 review, "Discussion Points" (decoding with a
  * KV cache by a kernel that splits the keys, then combines the parts).
  */

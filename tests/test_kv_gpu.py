@@ -64,6 +64,11 @@ def _check(attn, q, k, v, causal, n_split, scale):
     (1, 4, 2, 6, 555, 256, "fp16", 2),     # 12 rows, both halves of M
     (1, 16, 2, 2, 700, 192, "bf16", 5),    # 16 rows
     (2, 3, 3, 1, 130, 192, "fp16", 1),     # one row per key/value head
+    # wide head dims, 17-128 rows: groups of 16 rows on the decoding kernel
+    (1, 8, 1, 5, 900, 256, "bf16", 3),     # 40 rows: three groups, the last of 8
+    (1, 2, 1, 64, 300, 192, "fp16", 2),    # 128 rows: eight groups
+    (2, 4, 2, 9, 513, 256, "fp16", 1),     # 18 rows against a longer cache
+    (1, 1, 1, 100, 100, 192, "bf16", 3),   # Nq = Nk: the key split of attn_fwd_split
 ])
 def test_queries_against_a_cache(attn_lib, causal, B, Hq, Hkv, Nq, Nk, d, dtype, n_split):
     w = wl.Workload("kv", "fwd", B, Hq, Nk, d, dtype, causal, seed=Nq + Nk + d)

@@ -115,15 +115,15 @@ def test_wide_forward_deterministic(attn_lib):
 def test_wide_modes_not_built_are_rejected(attn_lib):
     """The key split, the key cache and packed variable-length batches are
     built for d <= 128 only, except on the decoding kernel's shapes (at most
-    16 query rows per key/value head): at d = 256 with 64 or 32 rows per head
+    128 query rows per key/value head): at d = 256 with 200 rows per head
     they return ATTN_ERR_UNSUPPORTED before any launch."""
     L = attn_lib.lib()
-    x = torch.zeros((1, 1, 64, 256), dtype=torch.bfloat16, device="cuda")
-    lse = torch.zeros((2, 1, 1, 64), dtype=torch.float32, device="cuda")
+    x = torch.zeros((1, 1, 256, 256), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((2, 1, 1, 256), dtype=torch.float32, device="cuda")
     p, pl = ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(lse.data_ptr())
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    assert L.attn_fwd_split(p, p, p, p, pl, 2, 1, 1, 64, 256, 1, 0.1, 1, s) == 2
-    assert L.attn_fwd_kv(p, p, p, p, pl, 1, 1, 1, 1, 32, 64, 256, 1, 0.1, 1, s) == 2
+    assert L.attn_fwd_split(p, p, p, p, pl, 2, 1, 1, 200, 256, 1, 0.1, 1, s) == 2
+    assert L.attn_fwd_kv(p, p, p, p, pl, 1, 1, 1, 1, 200, 256, 256, 1, 0.1, 1, s) == 2
     assert L.attn_fwd(p, p, p, p, pl, 1, 1, 64, 320, 1, 0.1, 1, s) == 2  # d = 320
     assert attn_lib.poll_status()[0] == 0
 
