@@ -118,13 +118,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Orders this thread's earlier generic-proxy shared-memory accesses (reads of
-// a staged tile) before its later async-proxy ones (a TMA copy into the same
-// buffer).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Named barrier that also returns the OR of `pred` over the participating
 // threads (a rendezvous that carries an abort bit both ways).
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred) {
