@@ -54,3 +54,31 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(attn, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         attn.lib()
+
+
+def test_argument_checks_return_before_any_launch(lib):
+    """Shapes the library does not take are refused on the host, before the
+    device is touched, so these calls run on a machine without a GPU (the
+    pointers are never dereferenced).  Status 1 = ATTN_ERR_INVALID_ARG,
+    2 = ATTN_ERR_UNSUPPORTED."""
+    p = ctypes.c_void_p(0x10000)       # 16-byte aligned, never read
+    bad = ctypes.c_void_p(0x10008)     # not 16-byte aligned
+    s = ctypes.c_void_p(0)
+    f = lib.attn_fwd_kv
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int,
+                                                                ctypes.c_void_p]
+    #   q  k  v  o  lse n_split B Hq Hkv Nq  Nk   d  causal scale bf16 stream
+    assert f(p, p, p, p, p, 1, 1, 1, 1, 200, 256, 256, 1, 0.1, 1, s) == 2  # 200 rows at d=256
+    assert f(p, p, p, p, p, 1, 1, 8, 1, 17, 300, 192, 1, 0.1, 1, s) == 2   # 136 rows at d=192
+    assert f(p, p, p, p, p, 1, 1, 1, 1, 4, 300, 80, 1, 0.1, 1, s) == 2     # d = 80
+    assert f(p, p, p, p, p, 1, 1, 1, 1, 300, 200, 128, 1, 0.1, 1, s) == 1  # Nq > Nk
+    assert f(p, p, p, p, p, 0, 1, 1, 1, 1, 200, 128, 1, 0.1, 1, s) == 1    # n_split = 0
+    assert f(p, p, p, p, p, 257, 1, 1, 1, 1, 200, 128, 1, 0.1, 1, s) == 1  # n_split > 256
+    assert f(p, p, p, p, p, 1, 1, 3, 2, 1, 200, 128, 1, 0.1, 1, s) == 1    # Hkv does not divide Hq
+    assert f(p, bad, p, p, p, 1, 1, 1, 1, 1, 200, 128, 1, 0.1, 1, s) == 1  # misaligned k
+    m = lib.attn_merge
+    m.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int] + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    assert m(p, p, 4, p, p, 1, 1, 1, 80, 1, s) == 2    # d = 80
+    assert m(p, p, 0, p, p, 1, 1, 1, 128, 1, s) == 1   # n_split = 0
+    assert m(p, p, 4, p, p, 0, 1, 1, 128, 1, s) == 1   # B = 0
