@@ -11,7 +11,8 @@ ragged sizes together, and runs one of three paths:
            oracle's full attention.
 A second set of cases draws decoding shapes (at most 16 query rows per
 key/value head, every head dim including 192 and 256, a ragged cache, 1-12
-key splits) for the key-cache forward and the merge.
+key splits) for the key-cache forward and the merge; at d = 192 and 256 a
+third of them take 17-128 rows (groups of 16 rows on the decoding kernel).
 Tolerances as everywhere: |O - O_ref| <= 2e-2, |LSE - LSE_ref| <= 5e-3,
 gradients <= 5e-2 * max |ref| per tensor (an all-zero reference, e.g. N = 1,
 bounds |g| <= 1e-3).
@@ -127,14 +128,17 @@ def test_random_feature_combination(attn_lib, seed):
     {"dense": _dense, "varlen": _varlen, "split": _split}[c["mode"]](attn_lib, c)
 
 
-DECODE_CASES = 24
+DECODE_CASES = 36
 
 
 def _draw_decode(seed):
     rng = np.random.default_rng(9000 + seed)
     G = int(rng.integers(1, 9))
     Nq = int(rng.integers(1, 16 // G + 1))  # G * Nq <= 16 rows per key/value head
-    return {"d": int(rng.choice([64, 96, 128, 192, 256])),
+    d = int(rng.choice([64, 96, 128, 192, 256]))
+    if d > 128 and seed % 3 == 0:
+        Nq = int(rng.integers(16 // G + 1, 128 // G + 1))  # 17-128 rows
+    return {"d": d,
             "dtype": str(rng.choice(["fp16", "bf16"])),
             "causal": bool(rng.integers(2)),
             "B": int(rng.integers(1, 3)),
