@@ -349,6 +349,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     for (int jj = j; jj < issued; ++jj) mbar_wait(bar(jj % NS), (jj / NS) & 1, dw, 62);
   }
 
+  // The key stream is done: a dependent launch (the merge) may start its
+  // launch now; it waits for this grid's completion before reading.
+  asm volatile("griddepcontrol.launch_dependents;");
+
   // Row sums over the four lanes of a row.
   lA += __shfl_xor_sync(0xffffffffu, lA, 1);
   lA += __shfl_xor_sync(0xffffffffu, lA, 2);

@@ -15,7 +15,11 @@
 // and O reads in flight together): the running maximum m rises with each
 // group and the sums gathered so far are scaled by exp(m_old - m_new), as in
 // the online softmax, so no separate pass over the LSEs waits on memory
-// first; grid-stride over rows; arithmetic in fp32.
+// first; grid-stride over rows; arithmetic in fp32.  Launched as a
+// programmatic dependent of the previous kernel on the stream: its launch
+// overlaps the tail of a producer that signals early (the decoding kernel
+// does, once its key stream is done), and it waits for that grid's
+// completion before its first read.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <atomic>
@@ -50,6 +54,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__
                                                     int n_split, long rows,
                                                     uint16_t* __restrict__ o,
                                                     float* __restrict__ lse) {
+  // launched as a programmatic dependent of the kernel that wrote the
+  // partials: wait until that grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   constexpr int kBatch = 4;  // splits whose rows are read together
@@ -132,10 +139,19 @@ cudaError_t launch_db(const MergeLaunch& a) {
   long blocks = (a.rows + 7) / 8;  // 8 warps (rows) per block
   const long cap = (long)a.num_sms * (per_sm > 0 ? per_sm : 1);
   if (blocks > cap) blocks = cap;
-  merge_kernel<D, BF16><<<(int)blocks, 256, 0, a.stream>>>(
-      static_cast<const uint16_t*>(a.o_part), a.lse_part, a.n_split, a.rows,
-      static_cast<uint16_t*>(a.o), a.lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, BF16>, static_cast<const uint16_t*>(a.o_part),
+                            static_cast<const float*>(a.lse_part), a.n_split, a.rows,
+                            static_cast<uint16_t*>(a.o), a.lse);
 }
 
 template <int D>

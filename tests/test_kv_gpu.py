@@ -175,6 +175,32 @@ def test_decode_at_the_wide_head_dims(attn_lib, d):
         assert np.max(np.abs(to64(L[b, h]) - L_ref[0, 0, 0])) <= LSE_TOL
 
 
+@pytest.mark.parametrize("kv_heads", [16, 2])
+def test_merge_right_after_the_decoding_kernel(attn_lib, kv_heads):
+    """The merge is launched as a programmatic dependent of the decoding
+    kernel (its launch overlaps the decoding kernel's tail): back to back on
+    the stream it gives the same bits as after a full synchronize."""
+    w = wl.DECODE_BF16_D128
+    inp = wl.make_decode_inputs(w, kv_heads=kv_heads)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    Op, Lp = attn_lib.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=True, scale=w.scale)
+    O, L = attn_lib.merge(Op, Lp)
+    for _ in range(3):
+        O.zero_()
+        Op.zero_()
+        attn_lib.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=True, scale=w.scale, out=Op, lse=Lp)
+        attn_lib.merge(Op, Lp, out=O, lse=L)
+    torch.cuda.synchronize()
+    O1, L1 = O.clone(), L.clone()
+    O.zero_()
+    attn_lib.fwd_kv(q, k, v, wl.DECODE_SPLITS, causal=True, scale=w.scale, out=Op, lse=Lp)
+    torch.cuda.synchronize()
+    attn_lib.merge(Op, Lp, out=O, lse=L)
+    torch.cuda.synchronize()
+    assert attn_lib.poll_status() == (0, 0)
+    assert torch.equal(O1, O) and torch.equal(L1, L)
+
+
 def test_more_queries_than_keys_is_rejected(attn_lib):
     L = attn_lib.lib()
     x = torch.zeros((1, 1, 256, 64), dtype=torch.bfloat16, device="cuda")
